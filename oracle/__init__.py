@@ -23,7 +23,7 @@ def lib():
         _lib = ctypes.CDLL(_build.build())
         P = ctypes.c_void_p
         i = ctypes.c_int
-        _lib.oracle_layer.argtypes = [P, i, i, i, i, i, i, P, P, P, P, P, P, P, P, i, P, i, i, P, P, P, P, P, P, P]
+        _lib.oracle_layer.argtypes = [P, i, i, i, i, i, i, P, P, P, P, P, P, P, P, i, P, i, i, P, P, P, P, P, P, P, P]
         _lib.oracle_layer.restype = i
         _lib.oracle_router_logits.argtypes = [P, i, i, P, P, i, P, i]
         _lib.oracle_topk_softmax.argtypes = [P, i, i, i, P, P]
@@ -35,6 +35,7 @@ def lib():
         _lib.oracle_weight_code.restype = i
         _lib.oracle_weight_value.argtypes = [P, P, i, i, i, i]
         _lib.oracle_weight_value.restype = ctypes.c_double
+        _lib.oracle_weight_column.argtypes = [P, P, i, i, i, P]
         _lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
         _lib.oracle_half_to_double.restype = ctypes.c_double
     return _lib
@@ -115,6 +116,13 @@ def dequantize_matrix(codes_e, scales_e, bits, N, K):
     return out
 
 
+def weight_column(codes_e, scales_e, bits, N, kk):
+    """Column kk (an input index) of one expert's dequantised [N, K] matrix, fp64."""
+    out = np.empty(N, np.float64)
+    lib().oracle_weight_column(_p(_c(codes_e, np.uint8)), _p(_c(scales_e, np.uint16)), bits, N, kk, _p(out))
+    return out
+
+
 def half_to_double(bits16: int) -> float:
     return lib().oracle_half_to_double(bits16)
 
@@ -152,11 +160,11 @@ def layer(x, Wr, bias, codes, scales, bits, k, residual=False, tokens=None, nthr
     b = None if bias is None else _c(bias, np.float32)
     out = dict(idx=np.empty((n, k), np.int32), w=np.empty((n, k), np.float32), y=np.empty((n, H), np.float32))
     if detail:
-        out.update(qh=np.empty((n, k, I), np.int8), sh=np.empty((n, k, I // 32), np.float32),
+        out.update(h=np.empty((n, k, I), np.float32), qh=np.empty((n, k, I), np.int8), sh=np.empty((n, k, I // 32), np.float32),
                    hdist=np.empty((n, k, I)), D=np.empty((n, k, H)))
     rc = lib().oracle_layer(_p(x), T, H, I, E, k, bits, _p(Wr), _p(b), _p(c[0]), _p(s[0]), _p(c[1]), _p(s[1]),
                             _p(c[2]), _p(s[2]), int(bool(residual)), _p(tokens), n, nthreads or default_threads(),
-                            _p(out["idx"]), _p(out["w"]), _p(out["y"]), _p(out.get("qh")), _p(out.get("sh")),
+                            _p(out["idx"]), _p(out["w"]), _p(out["y"]), _p(out.get("h")), _p(out.get("qh")), _p(out.get("sh")),
                             _p(out.get("hdist")), _p(out.get("D")))
     if rc != 0:
         raise ValueError("oracle_layer rejected its arguments")

@@ -264,6 +264,7 @@ typedef struct {
     int32_t *idx;  /* [n_tokens, k] */
     float *w;      /* [n_tokens, k] */
     float *y;      /* [n_tokens, H] */
+    float *h;      /* [n_tokens, k, I] or NULL */
     int8_t *qh;    /* [n_tokens, k, I] or NULL */
     float *sh;     /* [n_tokens, k, I/32] or NULL */
     double *hdist; /* [n_tokens, k, I] or NULL */
@@ -296,7 +297,7 @@ static void layer_token(const layer_job *J, int r)
                             J->codes[0] + e * Ecb_g, J->scales[0] + e * Esc_g,
                             J->codes[1] + e * Ecb_g, J->scales[1] + e * Esc_g,
                             J->codes[2] + e * Ecb_d, J->scales[2] + e * Esc_d,
-                            NULL, NULL, NULL,
+                            NULL, NULL, J->h ? J->h + rj * I : NULL,
                             J->qh ? J->qh + rj * I : NULL, J->sh ? J->sh + rj * (I / 32) : NULL,
                             J->hdist ? J->hdist + rj * I : NULL, D);
         for (int n = 0; n < H; ++n)
@@ -331,7 +332,7 @@ int oracle_layer(const float *x, int T, int H, int I, int E, int k, int bits,
                  const uint8_t *cd, const uint16_t *sd, int residual,
                  const int32_t *tokens, int n_tokens, int nthreads,
                  int32_t *idx_out, float *w_out, float *y_out,
-                 int8_t *qh_out, float *sh_out, double *hdist_out, double *D_out)
+                 float *h_out, int8_t *qh_out, float *sh_out, double *hdist_out, double *D_out)
 {
     if (H % 32 || I % 32 || k < 1 || k > E || (bits != 2 && bits != 3))
         return -1;
@@ -343,7 +344,7 @@ int oracle_layer(const float *x, int T, int H, int I, int E, int k, int bits,
     if (nthreads > n_tokens)
         nthreads = n_tokens > 0 ? n_tokens : 1;
     layer_job base = {x, T, H, I, E, k, bits, Wr, bias, {cg, cu, cd}, {sg, su, sd}, residual,
-                      tokens, n_tokens, idx_out, w_out, y_out, qh_out, sh_out, hdist_out, D_out, 0, 0};
+                      tokens, n_tokens, idx_out, w_out, y_out, h_out, qh_out, sh_out, hdist_out, D_out, 0, 0};
     layer_job *jobs = (layer_job *)malloc(sizeof(layer_job) * (size_t)nthreads);
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
     for (int i = 0; i < nthreads; ++i) {
@@ -404,4 +405,11 @@ int oracle_topk_softmax(const double *L, int T, int E, int k, int32_t *idx, floa
     for (int t = 0; t < T; ++t)
         oracle_topk_softmax_token(L + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
     return 0;
+}
+
+/* Column kk of one expert's dequantised [N, K] matrix (N values, fp64). */
+void oracle_weight_column(const uint8_t *codes, const uint16_t *scales, int bits, int N, int kk, double *out)
+{
+    for (int n = 0; n < N; ++n)
+        out[n] = oracle_weight_value(codes, scales, bits, N, n, kk);
 }

@@ -1,0 +1,530 @@
+// moeq.cu -- libmoeq: host side of the C ABI declared in include/moeq.h, and
+// the one translation unit that instantiates every kernel.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "combine.cuh"
+#include "common.cuh"
+#include "ffn_gemm.cuh"
+#include "ffn_gemv.cuh"
+#include "permute.cuh"
+#include "quant.cuh"
+#include "route.cuh"
+
+using namespace moeq;
+
+namespace {
+
+thread_local std::string g_err;
+
+// kernel tracing (moe_trace_events)
+thread_local cudaEvent_t *g_trace = nullptr;
+thread_local int g_trace_n = 0, g_trace_c = 0;
+
+// Under stream capture a plain cudaEventRecord only expresses a dependency;
+// cudaEventRecordExternal makes it an event-record node that fires on replay.
+void trace_record(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, s);
+}
+void trace_begin(cudaStream_t s) {
+    if (g_trace_n) trace_record(g_trace[g_trace_c], s);
+}
+void trace_end(cudaStream_t s) {
+    if (g_trace_n) {
+        trace_record(g_trace[g_trace_c + 1], s);
+        g_trace_c = (g_trace_c + 2) % g_trace_n;
+    }
+}
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int ok() {
+    g_err.clear();
+    return MOEQ_OK;
+}
+
+int cuda_check(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return MOEQ_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Token count up to which the routed experts run as GEMVs (auto mode).
+constexpr int kGemvMaxT = 64;
+// Token count up to which the decode fast path fuses routing and permutation.
+constexpr int kFusedRouteMaxT = kRouteTok;
+
+struct Layout {
+    size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, active, tiles, qx, sx,
+        ex, xhi, xlo, qh, sh, eh, hhi, hlo, total;
+};
+
+Layout layout(long long T, long long H, long long I, long long E, long long k) {
+    Layout L;
+    size_t off = 0;
+    auto take = [&](long long bytes) {
+        size_t o = off;
+        off += ((size_t)(bytes > 0 ? bytes : 0) + 255) & ~(size_t)255;
+        return o;
+    };
+    const long long P = T * k, W = (T + 31) / 32;
+    const long long max_tiles = (P + kTileN - 1) / kTileN + E;
+    L.ctrl = take(256);
+    L.logits = take(T * E * 4);
+    L.idx = take(P * 4);
+    L.w = take(P * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm_tok = take(P * 4);
+    L.perm_slot = take(P * 4);
+    L.inv = take(P * 4);
+    L.masks = take(E * W * 4);
+    L.prefix = take(E * W * 4);
+    L.active = take(E * 4);
+    L.tiles = take(max_tiles * (long long)sizeof(Tile));
+    L.qx = take(T * H);
+    L.sx = take(T * (H / 32) * 4);
+    L.ex = take(T * 4);
+    L.xhi = take(T * H * 2);
+    L.xlo = take(T * H * 2);
+    L.qh = take(P * I);
+    L.sh = take(P * (I / 32) * 4);
+    L.eh = take(P * 4);
+    L.hhi = take(P * I * 2);
+    L.hlo = take(P * I * 2);
+    L.total = off;
+    return L;
+}
+
+int check_shape(int T, int H, int I, int E, int k) {
+    if (T < 0) return fail(MOEQ_ERR_ARG, "T = %d < 0", T);
+    if (E < 1 || E > kMaxE) return fail(MOEQ_ERR_SHAPE, "E = %d outside [1, %d]", E, kMaxE);
+    if (k < 1 || k > E || k > kMaxK) return fail(MOEQ_ERR_SHAPE, "k = %d outside [1, min(E, %d)]", k, kMaxK);
+    if (H < 128 || H > 16384 || H % 128) return fail(MOEQ_ERR_SHAPE, "H = %d: need a multiple of 128 in [128, 16384]", H);
+    if (I < 128 || I > 4096 || I % 128) return fail(MOEQ_ERR_SHAPE, "I = %d: need a multiple of 128 in [128, 4096]", I);
+    if ((long long)T * k > (1ll << 26)) return fail(MOEQ_ERR_SHAPE, "T*k = %lld too large", (long long)T * k);
+    return MOEQ_OK;
+}
+
+#define REQ_PTR(p)                                                                                  \
+    do {                                                                                            \
+        if (!(p)) return fail(MOEQ_ERR_ARG, "%s is NULL", #p);                                      \
+        if (!aligned((p), 16)) return fail(MOEQ_ERR_ALIGN, "%s is not 16-byte aligned", #p);        \
+    } while (0)
+#define OPT_PTR(p)                                                                                  \
+    do {                                                                                            \
+        if ((p) && !aligned((p), 16)) return fail(MOEQ_ERR_ALIGN, "%s is not 16-byte aligned", #p); \
+    } while (0)
+
+int check_ws(void *ws, size_t ws_bytes, const Layout &L) {
+    if (!ws) return fail(MOEQ_ERR_ARG, "ws is NULL");
+    if (!aligned(ws, 256)) return fail(MOEQ_ERR_ALIGN, "ws is not 256-byte aligned");
+    if (ws_bytes < L.total) return fail(MOEQ_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+    return MOEQ_OK;
+}
+
+int check_weights(const moe_qweights *wq, int H, int I, int E) {
+    if (!wq) return fail(MOEQ_ERR_ARG, "weights is NULL");
+    if (wq->bits != 2 && wq->bits != 3) return fail(MOEQ_ERR_SHAPE, "bits = %d (need 2 or 3)", wq->bits);
+    if (wq->H != H || wq->I != I || wq->E != E)
+        return fail(MOEQ_ERR_ARG, "weights describe E=%d H=%d I=%d, call uses E=%d H=%d I=%d", wq->E, wq->H, wq->I,
+                    E, H, I);
+    for (int m = 0; m < 3; ++m) {
+        if (!wq->codes[m] || !wq->scales[m]) return fail(MOEQ_ERR_ARG, "weight matrix %d is NULL", m);
+        if (!aligned(wq->codes[m], 16) || !aligned(wq->scales[m], 16))
+            return fail(MOEQ_ERR_ALIGN, "weight matrix %d is not 16-byte aligned", m);
+    }
+    return MOEQ_OK;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+template <int PER>
+void launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t s) {
+    const int blocks = (T * 32 + 255) / 256;
+    topk_kernel<PER><<<blocks, 256, 0, s>>>(logits, T, E, k, idx, w);
+}
+
+void topk_dispatch(const float *logits, int T, int E, int k, int32_t *idx, float *w, cudaStream_t s) {
+    const int per = (E + 31) / 32;
+    if (per <= 1) launch_topk<1>(logits, T, E, k, idx, w, s);
+    else if (per <= 2) launch_topk<2>(logits, T, E, k, idx, w, s);
+    else if (per <= 4) launch_topk<4>(logits, T, E, k, idx, w, s);
+    else if (per <= 8) launch_topk<8>(logits, T, E, k, idx, w, s);
+    else if (per <= 16) launch_topk<16>(logits, T, E, k, idx, w, s);
+    else launch_topk<32>(logits, T, E, k, idx, w, s);
+}
+
+template <int PER>
+void launch_route_gemv(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
+                       int fuse, const DecodeTail &tail, cudaStream_t s) {
+    const int blocks = (E + kRouteRows - 1) / kRouteRows;
+    route_gemv_kernel<PER><<<blocks, 256, 0, s>>>(x, T, H, Wr, bias, E, logits, fuse, tail);
+}
+
+void route_gemv_dispatch(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
+                         int fuse, const DecodeTail &tail, cudaStream_t s) {
+    const int per = (E + 31) / 32;
+    if (per <= 1) launch_route_gemv<1>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+    else if (per <= 2) launch_route_gemv<2>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+    else if (per <= 4) launch_route_gemv<4>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+    else if (per <= 8) launch_route_gemv<8>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+    else if (per <= 16) launch_route_gemv<16>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+    else launch_route_gemv<32>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+}
+
+// Router logits + top-k (unfused).
+void route_unfused(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k, int32_t *idx,
+                   float *w, float *logits, cudaStream_t s) {
+    if (T <= kGemvMaxT) {
+        DecodeTail none{};
+        route_gemv_dispatch(x, T, H, Wr, bias, E, logits, 0, none, s);
+    } else {
+        dim3 grid((E + kSgBN - 1) / kSgBN, (T + kSgBM - 1) / kSgBM);
+        route_sgemm_kernel<<<grid, 256, 0, s>>>(x, T, H, Wr, bias, E, logits);
+    }
+    topk_dispatch(logits, T, E, k, idx, w, s);
+}
+
+template <int BITS>
+int launch_gemv(const GemvArgs &g, int T, int k, int E, cudaStream_t s) {
+    const size_t smem = gemv_smem_bytes(g.H);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_gemv_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "gemv smem attribute: %s", cudaGetErrorString(e));
+    }
+    const long long units = std::min<long long>((long long)T * k, E);
+    const long long blocks = units * (g.I / 32);
+    if (blocks == 0) return MOEQ_OK;
+    trace_begin(s);
+    ffn_gemv_kernel<BITS><<<(unsigned)blocks, 256, smem, s>>>(g);
+    trace_end(s);
+    return cuda_check("ffn_gemv_kernel");
+}
+
+template <bool GATEUP, int BITS>
+int launch_gemm(const GemmArgs &g, long long max_tiles, cudaStream_t s) {
+    using C = GemmCfg<GATEUP, BITS>;
+    cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel<GATEUP, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
+    const int MT = (GATEUP ? g.I : g.H) / kGmM;
+    const long long blocks = max_tiles * MT;
+    if (blocks == 0) return MOEQ_OK;
+    trace_begin(s);
+    ffn_gemm_kernel<GATEUP, BITS><<<(unsigned)blocks, 256, C::SMEM, s>>>(g);
+    trace_end(s);
+    return cuda_check("ffn_gemm_kernel");
+}
+
+// Experts over an existing permutation.  `plan_ready`: ctrl[1] / active were
+// already written by the fused decode routing.
+int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t *offsets, const int32_t *perm_tok,
+            const int32_t *perm_slot, const float *w, float *out_sorted, float *y, int residual, int mode,
+            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, bool plan_ready, cudaStream_t s) {
+    const int H = wq->H, I = wq->I, E = wq->E, bits = wq->bits;
+    const long long P = (long long)T * k;
+    if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
+    int *ctrl = at<int>(ws, L.ctrl);
+    if (y) {
+        const size_t n = (size_t)T * H;
+        const int blocks = (int)std::min<size_t>((n / 4 + 255) / 256, 148 * 16);
+        if (blocks > 0) init_y_kernel<<<blocks, 256, 0, s>>>(x, y, n, residual);
+    }
+    if (T == 0) return cuda_check("init_y_kernel");
+    if (!plan_ready)
+        plan_kernel<<<1, 1024, 0, s>>>(offsets, E, ctrl, at<int32_t>(ws, L.active), at<Tile>(ws, L.tiles));
+    if (int rc = cuda_check("plan_kernel")) return rc;
+    if (mode == MOEQ_MODE_GEMV) {
+        if (out_sorted) cudaMemsetAsync(out_sorted, 0, (size_t)P * H * sizeof(float), s);
+        GemvArgs g{};
+        g.x = x;
+        g.T = T;
+        g.H = H;
+        g.I = I;
+        g.E = E;
+        g.k = k;
+        for (int m = 0; m < 3; ++m) {
+            g.codes[m] = wq->codes[m];
+            g.scales[m] = wq->scales[m];
+        }
+        g.offsets = offsets;
+        g.perm_tok = perm_tok;
+        g.perm_slot = perm_slot;
+        g.w = w;
+        g.active = at<int32_t>(ws, L.active);
+        g.ctrl = ctrl;
+        g.y = y;
+        g.out_sorted = out_sorted;
+        g.qh_out = qh_out;
+        g.sh_out = sh_out;
+        return bits == 2 ? launch_gemv<2>(g, T, k, E, s) : launch_gemv<3>(g, T, k, E, s);
+    }
+    // grouped tensor-core GEMMs
+    int8_t *qx = at<int8_t>(ws, L.qx);
+    float *sx = at<float>(ws, L.sx);
+    int *ex = at<int>(ws, L.ex);
+    __half *xhi = at<__half>(ws, L.xhi), *xlo = at<__half>(ws, L.xlo);
+    int8_t *qh = qh_out ? qh_out : at<int8_t>(ws, L.qh);
+    float *sh = sh_out ? sh_out : at<float>(ws, L.sh);
+    int *eh = at<int>(ws, L.eh);
+    __half *hhi = at<__half>(ws, L.hhi), *hlo = at<__half>(ws, L.hlo);
+    quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, xhi, xlo, ex, nullptr, nullptr, nullptr);
+    if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
+    const long long max_tiles = (P + kTileN - 1) / kTileN + E;
+    GemmArgs g{};
+    g.T = T;
+    g.H = H;
+    g.I = I;
+    g.E = E;
+    g.k = k;
+    for (int m = 0; m < 3; ++m) {
+        g.codes[m] = wq->codes[m];
+        g.scales[m] = wq->scales[m];
+    }
+    g.tiles = at<Tile>(ws, L.tiles);
+    g.ctrl = ctrl;
+    g.perm_tok = perm_tok;
+    g.perm_slot = perm_slot;
+    g.w = w;
+    g.bhi = xhi;
+    g.blo = xlo;
+    g.brow_exp = ex;
+    g.qh = qh;
+    g.sh = sh;
+    int rc = bits == 2 ? launch_gemm<true, 2>(g, max_tiles, s) : launch_gemm<true, 3>(g, max_tiles, s);
+    if (rc) return rc;
+    quant_rows_kernel<<<(unsigned)P, 256, 0, s>>>(nullptr, I, nullptr, nullptr, hhi, hlo, eh, qh, sh, nullptr);
+    if ((rc = cuda_check("quant_rows_kernel(h)"))) return rc;
+    g.bhi = hhi;
+    g.blo = hlo;
+    g.brow_exp = eh;
+    g.y = y;
+    g.out_sorted = out_sorted;
+    return bits == 2 ? launch_gemm<false, 2>(g, max_tiles, s) : launch_gemm<false, 3>(g, max_tiles, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_last_error_string(void) { return g_err.c_str(); }
+
+const char *moe_version(void) { return "moeq 0.1.0 sm_103a"; }
+
+int moe_trace_events(void *const *events, int n) {
+    if (n < 0 || (n & 1) || (n > 0 && !events)) return fail(MOEQ_ERR_ARG, "need an even number of events");
+    static thread_local cudaEvent_t store[4096];
+    if (n > 4096) return fail(MOEQ_ERR_ARG, "at most 4096 trace events");
+    for (int i = 0; i < n; ++i) store[i] = (cudaEvent_t)events[i];
+    g_trace = n ? store : nullptr;
+    g_trace_n = n;
+    g_trace_c = 0;
+    return ok();
+}
+
+size_t moe_workspace_bytes(int T, int H, int I, int E, int k, int bits) {
+    if (check_shape(T, H, I, E, k) != MOEQ_OK || (bits != 2 && bits != 3)) return 0;
+    return layout(T, H, I, E, k).total;
+}
+
+int moe_route_topk(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k, int32_t *idx_out,
+                   float *w_out, void *ws, size_t ws_bytes, void *stream) {
+    if (int rc = check_shape(T, H, 128, E, k)) return rc;
+    REQ_PTR(x);
+    REQ_PTR(Wr);
+    OPT_PTR(bias);
+    REQ_PTR(idx_out);
+    REQ_PTR(w_out);
+    const Layout L = layout(T, H, 128, E, k);
+    if (ws_bytes < L.logits + (size_t)T * E * 4) return fail(MOEQ_ERR_WORKSPACE, "workspace too small for logits");
+    if (!ws || !aligned(ws, 256)) return fail(MOEQ_ERR_ALIGN, "ws missing or not 256-byte aligned");
+    if (T == 0) return ok();
+    cudaStream_t s = (cudaStream_t)stream;
+    route_unfused(x, T, H, Wr, bias, E, k, idx_out, w_out, at<float>(ws, L.logits), s);
+    if (int rc = cuda_check("moe_route_topk")) return rc;
+    return ok();
+}
+
+int moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts_out, int32_t *offsets_out,
+                int32_t *perm_tok_out, int32_t *perm_slot_out, int32_t *inv_out, void *ws, size_t ws_bytes,
+                void *stream) {
+    if (int rc = check_shape(T, 128, 128, E, k)) return rc;
+    REQ_PTR(counts_out);
+    REQ_PTR(offsets_out);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        cudaMemsetAsync(counts_out, 0, (size_t)E * 4, s);
+        cudaMemsetAsync(offsets_out, 0, (size_t)(E + 1) * 4, s);
+        if (int rc = cuda_check("moe_permute")) return rc;
+        return ok();
+    }
+    REQ_PTR(idx);
+    REQ_PTR(perm_tok_out);
+    REQ_PTR(perm_slot_out);
+    REQ_PTR(inv_out);
+    const Layout L = layout(T, 128, 128, E, k);
+    if (!ws || !aligned(ws, 256)) return fail(MOEQ_ERR_ALIGN, "ws missing or not 256-byte aligned");
+    if (ws_bytes < L.prefix + (size_t)E * ((T + 31) / 32) * 4) return fail(MOEQ_ERR_WORKSPACE, "workspace too small");
+    permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, at<unsigned>(ws, L.masks), at<int>(ws, L.prefix), counts_out,
+                                      offsets_out, perm_tok_out, perm_slot_out, inv_out);
+    if (int rc = cuda_check("permute_kernel")) return rc;
+    return ok();
+}
+
+int moe_quantize_act(const float *x, int T, int H, int8_t *q_out, float *s_out, void *stream) {
+    if (T < 0) return fail(MOEQ_ERR_ARG, "T < 0");
+    if (H < 32 || H % 32 || H > (1 << 20)) return fail(MOEQ_ERR_SHAPE, "H = %d must be a positive multiple of 32", H);
+    if (T == 0) return ok();
+    REQ_PTR(x);
+    REQ_PTR(q_out);
+    REQ_PTR(s_out);
+    quant_rows_kernel<<<T, 256, 0, (cudaStream_t)stream>>>(x, H, q_out, s_out, nullptr, nullptr, nullptr, nullptr,
+                                                            nullptr, nullptr);
+    if (int rc = cuda_check("quant_rows_kernel")) return rc;
+    return ok();
+}
+
+int moe_expert_ffn_q2(const float *x, int T, const moe_qweights *weights, int k, const int32_t *offsets,
+                      const int32_t *perm_tok, const int32_t *perm_slot, const float *w, float *out_sorted, float *y,
+                      int residual, int mode, int8_t *qh_out, float *sh_out, void *ws, size_t ws_bytes,
+                      void *stream) {
+    if (!weights) return fail(MOEQ_ERR_ARG, "weights is NULL");
+    const int H = weights->H, I = weights->I, E = weights->E;
+    if (int rc = check_shape(T, H, I, E, k)) return rc;
+    if (int rc = check_weights(weights, H, I, E)) return rc;
+    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
+    if (!out_sorted && !y) return fail(MOEQ_ERR_ARG, "need out_sorted or y");
+    OPT_PTR(out_sorted);
+    OPT_PTR(y);
+    OPT_PTR(qh_out);
+    OPT_PTR(sh_out);
+    if (T > 0) {
+        REQ_PTR(x);
+        REQ_PTR(offsets);
+        REQ_PTR(perm_tok);
+        REQ_PTR(perm_slot);
+        if (y) REQ_PTR(w);
+    }
+    const Layout L = layout(T, H, I, E, k);
+    if (int rc = check_ws(ws, ws_bytes, L)) return rc;
+    if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, out_sorted, y, residual, mode, qh_out,
+                         sh_out, ws, L, false, (cudaStream_t)stream))
+        return rc;
+    return ok();
+}
+
+int moe_combine(const float *out_sorted, const int32_t *inv, const float *w, int T, int k, int H,
+                const float *residual_x, float *y_out, void *stream) {
+    if (T < 0 || k < 1 || k > kMaxK) return fail(MOEQ_ERR_ARG, "bad T or k");
+    if (H < 4 || H % 4) return fail(MOEQ_ERR_SHAPE, "H = %d must be a positive multiple of 4", H);
+    if (T == 0) return ok();
+    REQ_PTR(out_sorted);
+    REQ_PTR(inv);
+    REQ_PTR(w);
+    OPT_PTR(residual_x);
+    REQ_PTR(y_out);
+    combine_kernel<<<T, 256, 0, (cudaStream_t)stream>>>(out_sorted, inv, w, k, H, residual_x, y_out);
+    if (int rc = cuda_check("combine_kernel")) return rc;
+    return ok();
+}
+
+int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias, const moe_qweights *weights, int k,
+                      int residual, float *y_out, int32_t *idx_out, float *w_out, int mode, void *ws,
+                      size_t ws_bytes, void *stream) {
+    if (!weights) return fail(MOEQ_ERR_ARG, "weights is NULL");
+    const int H = weights->H, I = weights->I, E = weights->E;
+    if (int rc = check_shape(T, H, I, E, k)) return rc;
+    if (int rc = check_weights(weights, H, I, E)) return rc;
+    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
+    OPT_PTR(bias);
+    OPT_PTR(idx_out);
+    OPT_PTR(w_out);
+    if (T > 0) {
+        REQ_PTR(x);
+        REQ_PTR(Wr);
+        REQ_PTR(y_out);
+    }
+    const Layout L = layout(T, H, I, E, k);
+    if (int rc = check_ws(ws, ws_bytes, L)) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) return ok();
+    int32_t *idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
+    float *w = w_out ? w_out : at<float>(ws, L.w);
+    int32_t *counts = at<int32_t>(ws, L.counts), *offsets = at<int32_t>(ws, L.offsets);
+    int32_t *perm_tok = at<int32_t>(ws, L.perm_tok), *perm_slot = at<int32_t>(ws, L.perm_slot);
+    int32_t *inv = at<int32_t>(ws, L.inv);
+    if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
+    if (T <= kFusedRouteMaxT && mode == MOEQ_MODE_GEMV) {
+        // decode: router + top-k + permutation + y init in one kernel, then the experts
+        DecodeTail tail{k, idx, w, counts, offsets, perm_tok, perm_slot, inv, at<int32_t>(ws, L.active),
+                        at<int>(ws, L.ctrl), y_out, residual};
+        route_gemv_dispatch(x, T, H, Wr, bias, E, at<float>(ws, L.logits), 1, tail, s);
+        if (int rc = cuda_check("route_gemv_kernel(fused)")) return rc;
+        GemvArgs g{};
+        g.x = x;
+        g.T = T;
+        g.H = H;
+        g.I = I;
+        g.E = E;
+        g.k = k;
+        for (int m = 0; m < 3; ++m) {
+            g.codes[m] = weights->codes[m];
+            g.scales[m] = weights->scales[m];
+        }
+        g.offsets = offsets;
+        g.perm_tok = perm_tok;
+        g.perm_slot = perm_slot;
+        g.w = w;
+        g.active = at<int32_t>(ws, L.active);
+        g.ctrl = at<int>(ws, L.ctrl);
+        g.y = y_out;
+        int rc = weights->bits == 2 ? launch_gemv<2>(g, T, k, E, s) : launch_gemv<3>(g, T, k, E, s);
+        if (rc) return rc;
+        return ok();
+    }
+    route_unfused(x, T, H, Wr, bias, E, k, idx, w, at<float>(ws, L.logits), s);
+    if (int rc = cuda_check("route")) return rc;
+    permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, at<unsigned>(ws, L.masks), at<int>(ws, L.prefix), counts, offsets,
+                                      perm_tok, perm_slot, inv);
+    if (int rc = cuda_check("permute_kernel")) return rc;
+    if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, nullptr, y_out, residual, mode, nullptr,
+                         nullptr, ws, L, false, s))
+        return rc;
+    return ok();
+}
+
+int moe_get_device_status(void *stream, int *status_out) {
+    if (!status_out) return fail(MOEQ_ERR_ARG, "status_out is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+    int st = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&st, g_status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    *status_out = st;
+    if (st) return fail(MOEQ_ERR_DEVICE, "device status 0x%x", st);
+    return ok();
+}
+
+}  // extern "C"

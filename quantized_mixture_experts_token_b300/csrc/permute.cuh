@@ -1,0 +1,105 @@
+// permute.cuh -- deterministic token-to-expert grouping, and the work plan
+// (active experts, 128-token tiles) the expert kernels run over.
+//
+// The pages' prompt path multiplies each expert once for all of a chunk's
+// tokens that picked it ("Strata - the details", "Speed (measured)"), which
+// needs the (token, slot) pairs grouped by expert.
+#pragma once
+
+#include "common.cuh"
+
+namespace moeq {
+
+// Single CTA, 1024 threads.  Pair p = (t, j) sets bit t of its expert's token
+// bitmap; an expert's count is the popcount of its bitmap and the rank of
+// token t inside it is the popcount of the bits below t.  Ranks therefore
+// follow token order by construction (a stable counting sort) and never
+// depend on the order in which atomics land.  k distinct experts per token
+// make (e, t) unique.
+__global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict__ idx, int T, int k, int E,
+                                                       unsigned *masks /* [E][W] */, int *prefix /* [E][W] */,
+                                                       int32_t *counts, int32_t *offsets, int32_t *perm_tok,
+                                                       int32_t *perm_slot, int32_t *inv) {
+    __shared__ int s_off[kMaxE];
+    __shared__ int s_scan[33];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int W = (T + 31) / 32;
+    const size_t nm = (size_t)E * W;
+    for (size_t i = tid; i < nm; i += nt) masks[i] = 0u;
+    __syncthreads();
+    const int P = T * k;
+    for (int p = tid; p < P; p += nt) {
+        const int e = idx[p], t = p / k;
+        if (e < 0 || e >= E) {
+            set_status(MOEQ_STATUS_BAD_INDEX);
+            continue;
+        }
+        atomicOr(&masks[(size_t)e * W + (t >> 5)], 1u << (t & 31));
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += nt) {
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            prefix[(size_t)e * W + w] = run;
+            run += __popc(__ldcg(&masks[(size_t)e * W + w]));
+        }
+        counts[e] = run;
+        s_off[e] = run;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(s_off, E, s_scan);
+    for (int e = tid; e < E; e += nt) offsets[e] = s_off[e];
+    if (tid == 0) offsets[E] = total;
+    __syncthreads();
+    for (int p = tid; p < P; p += nt) {
+        const int e = idx[p], t = p / k, j = p - t * k;
+        if (e < 0 || e >= E) continue;
+        const size_t wi = (size_t)e * W + (t >> 5);
+        const int pos = s_off[e] + __ldcg(&prefix[wi]) + __popc(__ldcg(&masks[wi]) & ((1u << (t & 31)) - 1u));
+        perm_tok[pos] = t;
+        perm_slot[pos] = j;
+        inv[p] = pos;
+    }
+}
+
+// Work plan from offsets: the list of experts with at least one pair, and the
+// list of (expert, first sorted position, rows) tiles of up to kTileN pairs.
+constexpr int kTileN = 128;
+
+struct Tile {
+    int e, p0, n, pad;
+};
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int E, int *ctrl,
+                                                    int32_t *active, Tile *tiles) {
+    __shared__ int s_act[kMaxE];
+    __shared__ int s_til[kMaxE];
+    __shared__ int s_scan[33];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int c = offsets[e + 1] - offsets[e];
+        s_act[e] = c > 0;
+        s_til[e] = (c + kTileN - 1) / kTileN;
+    }
+    __syncthreads();
+    const int n_active = block_exclusive_scan(s_act, E, s_scan);
+    const int n_tiles = block_exclusive_scan(s_til, E, s_scan);
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int o = offsets[e], c = offsets[e + 1] - o;
+        if (c > 0) active[s_act[e]] = e;
+        for (int i = 0; i * kTileN < c; ++i) {
+            Tile tl;
+            tl.e = e;
+            tl.p0 = o + i * kTileN;
+            tl.n = min(kTileN, c - i * kTileN);
+            tl.pad = 0;
+            tiles[s_til[e] + i] = tl;
+        }
+    }
+    if (tid == 0) {
+        ctrl[1] = n_active;
+        ctrl[2] = n_tiles;
+    }
+}
+
+}  // namespace moeq

@@ -1,0 +1,70 @@
+// quant.cuh -- per-32-block int8 activation quantisation (the quantised
+// activations of the pages' MMQ / fused int8 prompt-expert kernels, "Strata -
+// the details", "Speed (measured)"), plus the fp16 hi/lo operand split the
+// tensor-core expert GEMM consumes.
+#pragma once
+
+#include "common.cuh"
+
+namespace moeq {
+
+// One CTA (256 threads) per row of n values (n multiple of 32).  Warp w
+// quantises blocks w, w+8, ...; lane i holds element i of the block.
+// Optional outputs: hi/lo fp16 rows of q*s*2^-e with e = row_exponent(max s).
+// `src_q`/`src_s` non-null: the row is already quantised (only the split runs).
+__global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict__ v, int n, int8_t *q_out,
+                                                         float *s_out, __half *hi, __half *lo, int *e_out,
+                                                         const int8_t *__restrict__ src_q,
+                                                         const float *__restrict__ src_s,
+                                                         const int32_t *__restrict__ row_map) {
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nb = n / 32;
+    __shared__ float s_max[8];
+    const int8_t *qrow;
+    const float *srow;
+    float smax = 0.f;
+    if (src_q) {
+        qrow = src_q + (size_t)row * n;
+        srow = src_s + (size_t)row * nb;
+        for (int b = tid; b < nb; b += blockDim.x) smax = fmaxf(smax, srow[b]);
+    } else {
+        const size_t src_row = row_map ? (size_t)row_map[row] : (size_t)row;
+        const float *vr = v + src_row * n;
+        int8_t *qr = q_out + (size_t)row * n;
+        float *sr = s_out + (size_t)row * nb;
+        for (int b = warp; b < nb; b += 8) {
+            const float val = vr[32 * b + lane];
+            const float s = block_scale(warp_absmax(val));
+            qr[32 * b + lane] = (int8_t)block_code(val, s);
+            if (lane == 0) sr[b] = s;
+            smax = fmaxf(smax, s);
+        }
+        qrow = qr;
+        srow = sr;
+    }
+    if (!hi) return;
+    // row maximum of the block scales -> exponent
+    for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+    if (lane == 0) s_max[warp] = smax;
+    __syncthreads();  // also orders this CTA's q/s stores before the re-reads below
+    float m = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = fmaxf(m, s_max[w]);
+    const int e = row_exponent(m);
+    if (tid == 0 && e_out) e_out[row] = e;
+    const float inv = exp2i(-e);
+    __half *hr = hi + (size_t)row * n;
+    __half *lr = lo + (size_t)row * n;
+    for (int i = 2 * tid; i < n; i += 2 * blockDim.x) {
+        const float s = srow[i / 32] * inv;
+        const float v0 = (float)qrow[i] * s, v1 = (float)qrow[i + 1] * s;
+        __half h0, l0, h1, l1;
+        split_hi_lo(v0, h0, l0);
+        split_hi_lo(v1, h1, l1);
+        *reinterpret_cast<__half2 *>(hr + i) = __halves2half2(h0, h1);
+        *reinterpret_cast<__half2 *>(lr + i) = __halves2half2(l0, l1);
+    }
+}
+
+}  // namespace moeq

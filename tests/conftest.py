@@ -19,6 +19,9 @@ def cuda_lib():
 
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
     import quantized_mixture_experts_token_b300 as moeq
 
     return moeq

@@ -1,0 +1,277 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: activation quantisation, routing indices, the permutation.
+Routing weights within W_REL relative: w_j = exp(L_j - L_0) / sum, so an error
+dL in every fp32 logit moves w_j by at most about 2 * max|dL| * w_j; fp32
+sums of H = 2048 products of N(0,1) x N(0,0.02) values carry |dL| of a few
+1e-6, hence W_REL = 1e-5.  Layer outputs within 2e-3 x RMS(output) (max
+abs error), allowing only the alternative int8 roundings of SwiGLU values that
+the oracle itself reports as lying within DELTA of a rounding boundary (in
+units of the quantisation step).  DELTA follows from each path's arithmetic:
+the GEMV path forms G and U from exact integer block dots with fp32 FMAs
+(relative error ~1e-7, so |dh/s| <= 127 * 1e-7 * few << 1e-3); the tensor-core
+path accumulates 2 * H / 16 = 256 MMAs of K = 16 in the fp32 TMEM accumulator,
+which rounds toward zero at each step: relative error up to 256 * 2^-24 per
+accumulator (~1.5e-5, measured 2.7e-5 on G*U), i.e. |dh/s| up to 127 * 3e-5
+~ 4e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle.checks import compare_layer_output, margin_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+W_REL = 1e-5
+DELTA = {1: 1e-3, 2: 4e-3}  # GEMV, tensor-core GEMM
+
+
+def _w_close(w_dev, w_ref):
+    w_dev = np.asarray(w_dev, np.float64)
+    w_ref = np.asarray(w_ref, np.float64)
+    return bool((np.abs(w_dev - w_ref) <= W_REL * w_ref + 1e-7).all())
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+class LayerCase:
+    """A layer on the device plus host copies for the oracle."""
+
+    def __init__(self, shape, seed=0, skew=False, device="cuda"):
+        self.shape = shape
+        self.layer = synth.make_layer(shape, seed=seed, device=device, skew=skew)
+        self.np = self.layer.numpy()
+        self.dev = self.layer.to(_dev())
+        import quantized_mixture_experts_token_b300 as moeq
+
+        self.W = moeq.ExpertWeights.from_layer(self.dev)
+
+    def x(self, T, seed=1, stream=0, margin=True):
+        x = synth.make_x(T, self.shape.H, seed=seed, stream=stream)
+        if margin and T > 0:
+            x = margin_inputs(x, self.np[0], self.np[1], self.shape.k, seed)
+        return x
+
+    def oracle(self, x, tokens=None, residual=False):
+        Wr, b, c, s = self.np
+        return oracle.layer(x.numpy(), Wr, b, c, s, self.shape.bits, self.shape.k, residual=residual,
+                            tokens=tokens, detail=True)
+
+    def check_y(self, y_dev, ref, rms=None, delta=DELTA[2]):
+        c, s = self.np[2][2], self.np[3][2]
+        return compare_layer_output(y_dev, ref, c, s, self.shape.bits, tol=TOL, rms=rms, delta=delta)
+
+
+@pytest.fixture(scope="module")
+def tiny(cuda_lib):
+    return LayerCase(synth.TINY, seed=0, device="cpu")
+
+
+@pytest.fixture(scope="module")
+def full(cuda_lib):
+    return LayerCase(synth.FULL, seed=0, device="cuda")
+
+
+@pytest.fixture(scope="module")
+def full_skew(cuda_lib):
+    return LayerCase(synth.FULL, seed=2, skew=True, device="cuda")
+
+
+def _ws(moeq, T, shape):
+    return moeq.workspace(T, shape.H, shape.I, shape.E, shape.k, shape.bits, device=_dev())
+
+
+# ------------------------------------------------------------ quantiser
+
+
+@pytest.mark.parametrize("T,H", [(3, 128), (64, 256), (4096, 2048)])
+def test_quantize_act_bit_exact(cuda_lib, T, H):
+    x = synth.make_x(T, H, seed=T) * 3
+    x[0, :32] = torch.tensor([127, 2.5, 3.5, -2.5, -0.5, 0.5, 1.5, -127] + [0.0] * 24)  # exact ties
+    x[0, 32:64] = 0.0  # a zero block
+    if T > 1:
+        x[1] *= 1e-30  # tiny scales
+    q, s = cuda_lib.quantize_act(x.to(_dev()))
+    qo, so = oracle.quantize_block32(x.numpy())
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+
+
+# ---------------------------------------------------------------- routing
+
+
+def _check_routing(case, x, idx, w):
+    L = oracle.router_logits(x.numpy(), case.np[0], case.np[1])
+    io, wo = oracle.topk_softmax(L, case.shape.k)
+    assert np.array_equal(idx.cpu().numpy(), io)
+    assert _w_close(w.cpu().numpy(), wo)
+    return io
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 200])
+def test_route_topk_tiny(tiny, cuda_lib, T):
+    x = tiny.x(T, seed=T)
+    ws = _ws(cuda_lib, T, tiny.shape)
+    idx, w = cuda_lib.route_topk(x.to(_dev()), tiny.dev.Wr, None, tiny.shape.k, ws)
+    _check_routing(tiny, x, idx, w)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64, 4096])
+def test_route_topk_full(full, full_skew, cuda_lib, T):
+    for case in (full, full_skew):
+        x = case.x(T, seed=10 + T)
+        ws = _ws(cuda_lib, T, case.shape)
+        idx, w = cuda_lib.route_topk(x.to(_dev()), case.dev.Wr, case.dev.bias, case.shape.k, ws)
+        _check_routing(case, x, idx, w)
+
+
+# ------------------------------------------------------------- permutation
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 512, 10), (8, 512, 10), (64, 16, 2), (1000, 7, 3), (4096, 512, 10),
+                                   (33, 1024, 32), (4096, 16, 2)])
+def test_permute_bit_exact(cuda_lib, T, E, k):
+    rng = np.random.default_rng(T * 31 + E)
+    # skewed expert popularity with some experts never chosen
+    p = rng.zipf(1.3, size=E).astype(np.float64)
+    p[rng.random(E) < 0.1] = 0
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, k, replace=False, p=p if (p > 0).sum() >= k else None) for _ in range(T)])
+    idx = idx.astype(np.int32)
+    ws = cuda_lib.workspace(T, 128, 128, E, k, device=_dev())
+    out = cuda_lib.permute(torch.from_numpy(idx).to(_dev()), E, ws)
+    ref = oracle.permute(idx, E)
+    for key in ("counts", "offsets", "perm_tok", "perm_slot", "inv"):
+        assert np.array_equal(out[key].cpu().numpy().reshape(ref[key].shape), ref[key]), key
+
+
+# ------------------------------------------------------------------ experts
+
+
+def _expert_case(case, cuda_lib, T, mode, residual=False, seed=5):
+    x = case.x(T, seed=seed)
+    xd = x.to(_dev())
+    ws = _ws(cuda_lib, T, case.shape)
+    idx, w = cuda_lib.route_topk(xd, case.dev.Wr, case.dev.bias, case.shape.k, ws)
+    perm = cuda_lib.permute(idx, case.shape.E, ws)
+    out = cuda_lib.expert_ffn(xd, case.W, case.shape.k, perm, w, want_y=True, want_sorted=True,
+                              residual=residual, mode=mode, want_h=True, ws=ws)
+    torch.cuda.synchronize()
+    return x, idx, w, perm, out
+
+
+def _check_h_codes(ref, qh_dev, sh_dev, inv, delta):
+    """Device int8 SwiGLU codes equal the oracle's except at oracle-reported near-ties (by one step)."""
+    n, k, I = ref["qh"].shape
+    q = qh_dev[inv.reshape(-1)].reshape(n, k, I).astype(np.int32)
+    s = sh_dev[inv.reshape(-1)].reshape(n, k, I // 32)
+    diff = q - ref["qh"].astype(np.int32)
+    bad = diff != 0
+    assert (np.abs(diff) <= 1).all()
+    assert (ref["hdist"][bad] < delta).all(), "a code differs away from a rounding boundary"
+    assert np.allclose(s, ref["sh"], rtol=delta / 64, atol=0)
+    return int(bad.sum())
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("T", [64, 600])
+def test_expert_ffn_tiny(tiny, cuda_lib, mode, T):
+    x, idx, w, perm, out = _expert_case(tiny, cuda_lib, T, mode)
+    ref = tiny.oracle(x)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    _check_h_codes(ref, out["qh"].cpu().numpy(), out["sh"].cpu().numpy(), perm["inv"].cpu().numpy(), DELTA[mode])
+    tiny.check_y(out["y"].cpu().numpy(), ref, delta=DELTA[mode])
+    # the per-pair outputs combined on the device reproduce y
+    y2 = cuda_lib.combine(out["out_sorted"], perm["inv"], w)
+    assert np.abs(y2.cpu().numpy() - out["y"].cpu().numpy()).max() <= 1e-5 * float(out["y"].abs().max())
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_expert_ffn_full_sampled(full_skew, cuda_lib, mode):
+    T = 4096 if mode == 2 else 256
+    x, idx, w, perm, out = _expert_case(full_skew, cuda_lib, T, mode, seed=7)
+    counts = perm["counts"].cpu().numpy()
+    assert (counts == 0).any(), "the skewed router must leave some experts without tokens"
+    tokens = np.random.default_rng(0).choice(T, 96, replace=False).astype(np.int32)
+    ref = full_skew.oracle(x, tokens=tokens)
+    assert np.array_equal(idx.cpu().numpy()[tokens], ref["idx"])
+    inv = perm["inv"].cpu().numpy()[tokens]
+    _check_h_codes(ref, out["qh"].cpu().numpy(), out["sh"].cpu().numpy(), inv, DELTA[mode])
+    full_skew.check_y(out["y"].cpu().numpy()[tokens], ref, delta=DELTA[mode])
+
+
+# -------------------------------------------------------------- whole layer
+
+
+@pytest.mark.parametrize("T", [1, 8, 16, 64])
+def test_layer_forward_decode_full(full, cuda_lib, T):
+    x = full.x(T, seed=100 + T)
+    ws = _ws(cuda_lib, T, full.shape)
+    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), full.W, full.dev.Wr, None, full.shape.k, ws, want_routing=True)
+    torch.cuda.synchronize()
+    ref = full.oracle(x)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert _w_close(w.cpu().numpy(), ref["w"])
+    full.check_y(y.cpu().numpy(), ref, delta=DELTA[1])
+    # a second call on the same workspace (re-armed counters) gives the same result
+    y2 = cuda_lib.layer_forward(x.to(_dev()), full.W, full.dev.Wr, None, full.shape.k, ws)
+    torch.cuda.synchronize()
+    assert np.abs(y2.cpu().numpy() - y.cpu().numpy()).max() <= 1e-6 * float(y.abs().max())
+
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_layer_forward_prefill_full(full_skew, cuda_lib, residual):
+    T = 4096
+    x = full_skew.x(T, seed=200)
+    ws = _ws(cuda_lib, T, full_skew.shape)
+    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), full_skew.W, full_skew.dev.Wr, full_skew.dev.bias,
+                                       full_skew.shape.k, ws, residual=residual, want_routing=True)
+    torch.cuda.synchronize()
+    tokens = np.random.default_rng(1).choice(T, 64, replace=False).astype(np.int32)
+    ref = full_skew.oracle(x, tokens=tokens, residual=residual)
+    assert np.array_equal(idx.cpu().numpy()[tokens], ref["idx"])
+    full_skew.check_y(y.cpu().numpy()[tokens], ref)
+    assert cuda_lib.device_status() == 0
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_layer_forward_tiny_modes(tiny, cuda_lib, mode):
+    T = 4096 if mode == 2 else 256
+    x = tiny.x(T, seed=300)
+    ws = _ws(cuda_lib, T, tiny.shape)
+    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), tiny.W, tiny.dev.Wr, None, tiny.shape.k, ws, mode=mode,
+                                       want_routing=True)
+    torch.cuda.synchronize()
+    ref = tiny.oracle(x)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    tiny.check_y(y.cpu().numpy(), ref, delta=DELTA[mode])
+
+
+def test_zero_tokens(tiny, cuda_lib):
+    ws = _ws(cuda_lib, 0, tiny.shape)
+    x = torch.zeros(0, tiny.shape.H, device=_dev())
+    y = cuda_lib.layer_forward(x, tiny.W, tiny.dev.Wr, None, tiny.shape.k, ws)
+    assert y.shape == (0, tiny.shape.H)
+
+
+def test_zero_input_gives_zero_output(tiny, cuda_lib):
+    T = 32
+    x = torch.zeros(T, tiny.shape.H)
+    ws = _ws(cuda_lib, T, tiny.shape)
+    for mode in (1, 2):
+        y, idx, w = cuda_lib.layer_forward(x.to(_dev()), tiny.W, tiny.dev.Wr, None, tiny.shape.k, ws, mode=mode,
+                                           want_routing=True)
+        torch.cuda.synchronize()
+        assert not y.cpu().numpy().any()
+        assert idx.cpu().numpy().tolist() == [[0, 1]] * T
+        assert np.allclose(w.cpu().numpy(), 0.5)
+
+
+def test_device_status_clean(cuda_lib):
+    assert cuda_lib.device_status() == 0
