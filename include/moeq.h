@@ -110,6 +110,31 @@ int moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts_out, in
                 void *stream);
 
 /*
+ * moe_permute without a workspace.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory --
+ * for example code embedded in a host framework that owns every device
+ * allocation, or a hot path that must never reach the CUDA allocator -- and so
+ * cannot provide the `ws` that moe_permute needs.
+ *
+ * Same arguments, outputs and results as moe_permute, bit for bit.  Its
+ * scratch (the per-expert token bitmaps and their prefix counts) lives in one
+ * fixed 512 KiB array in device memory that the library declares statically;
+ * every GPU that loads the library holds that array until the process exits.
+ * Limit: E * ceil(T / 32) <= 65536 (for E = 512 that is T <= 4096); larger
+ * sizes return MOEQ_ERR_SHAPE and launch nothing.  The call allocates and
+ * frees nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any CUDA stream capture.  All calls share the one array, so calls
+ * whose kernels may overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.  Each call clears the part of
+ * the array it needs, so no state carries over from the previous call.
+ */
+int moe_permute_noalloc(const int32_t *idx, int T, int k, int E, int32_t *counts_out, int32_t *offsets_out,
+                        int32_t *perm_tok_out, int32_t *perm_slot_out, int32_t *inv_out, void *stream);
+
+/*
  * Activation quantisation to int8 per 32-element block (the quantised-
  * activation prompt-expert kernels, "Strata - the details", "Speed
  * (measured)"): for each block, in fp32, s = amax/127 (IEEE division),

@@ -24,7 +24,7 @@ STATUS_WAIT_TIMEOUT, STATUS_BAD_INDEX = 0x1, 0x2
 
 # Function names of the C ABI (include/moeq.h).
 ABI_FUNCTIONS = (
-    "moe_route_topk", "moe_permute", "moe_quantize_act", "moe_expert_ffn_q2", "moe_combine",
+    "moe_route_topk", "moe_permute", "moe_permute_noalloc", "moe_quantize_act", "moe_expert_ffn_q2", "moe_combine",
     "moe_layer_forward", "moe_workspace_bytes", "moe_get_device_status", "moe_last_error_string",
     "moe_trace_events", "moe_version",
 )
@@ -54,6 +54,7 @@ def lib() -> ctypes.CDLL:
         P, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         L.moe_route_topk.argtypes = [P, i, i, P, P, i, i, P, P, P, sz, P]
         L.moe_permute.argtypes = [P, i, i, i, P, P, P, P, P, P, sz, P]
+        L.moe_permute_noalloc.argtypes = [P, i, i, i, P, P, P, P, P, P]
         L.moe_quantize_act.argtypes = [P, i, i, P, P, P]
         L.moe_expert_ffn_q2.argtypes = [P, i, ctypes.POINTER(QWeights), i, P, P, P, P, P, P, i, i, P, P, P, sz, P]
         L.moe_combine.argtypes = [P, P, P, i, i, i, P, P, P]
@@ -156,6 +157,25 @@ def permute(idx, E, ws):
                inv=torch.empty(max(T, 1), k, dtype=torch.int32, device=dev))
     _check(lib().moe_permute(_ptr(idx), T, k, E, _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm_tok"]),
                              _ptr(out["perm_slot"]), _ptr(out["inv"]), _ptr(ws), ws.numel(), _stream(dev)))
+    out["perm_tok"] = out["perm_tok"][: T * k]
+    out["perm_slot"] = out["perm_slot"][: T * k]
+    out["inv"] = out["inv"][:T]
+    return out
+
+
+def permute_noalloc(idx, E):
+    """moe_permute without a workspace: its scratch is a fixed array inside the
+    library, for callers that cannot allocate device memory (outputs are
+    allocated here only because this wrapper returns torch tensors)."""
+    T, k = idx.shape
+    dev = idx.device
+    out = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+               perm_tok=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+               perm_slot=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+               inv=torch.empty(max(T, 1), k, dtype=torch.int32, device=dev))
+    _check(lib().moe_permute_noalloc(_ptr(idx), T, k, E, _ptr(out["counts"]), _ptr(out["offsets"]),
+                                     _ptr(out["perm_tok"]), _ptr(out["perm_slot"]), _ptr(out["inv"]), _stream(dev)))
     out["perm_tok"] = out["perm_tok"][: T * k]
     out["perm_slot"] = out["perm_slot"][: T * k]
     out["inv"] = out["inv"][:T]

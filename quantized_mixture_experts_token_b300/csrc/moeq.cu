@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "combine.cuh"
@@ -324,6 +325,33 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     return bits == 2 ? launch_gemm<false, 2>(g, max_tiles, s) : launch_gemm<false, 3>(g, max_tiles, s);
 }
 
+// Scratch of moe_permute_noalloc: token bitmaps [E][W] then prefix counts
+// [E][W], W = ceil(T/32), each at most kNoAllocWords 32-bit words.
+constexpr size_t kNoAllocWords = 65536;
+__device__ __align__(256) unsigned g_permute_scratch[2 * kNoAllocWords];
+
+// Device address of g_permute_scratch, looked up once per device ordinal.
+constexpr int kMaxDevices = 64;
+void *g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+int noalloc_scratch(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOEQ_ERR_ARG, "device ordinal %d not supported", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_permute_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(MOEQ_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<unsigned *>(g_scratch_addr[dev]);
+    return MOEQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -389,6 +417,35 @@ int moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts_out, in
     permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, at<unsigned>(ws, L.masks), at<int>(ws, L.prefix), counts_out,
                                       offsets_out, perm_tok_out, perm_slot_out, inv_out);
     if (int rc = cuda_check("permute_kernel")) return rc;
+    return ok();
+}
+
+int moe_permute_noalloc(const int32_t *idx, int T, int k, int E, int32_t *counts_out, int32_t *offsets_out,
+                        int32_t *perm_tok_out, int32_t *perm_slot_out, int32_t *inv_out, void *stream) {
+    if (int rc = check_shape(T, 128, 128, E, k)) return rc;
+    REQ_PTR(counts_out);
+    REQ_PTR(offsets_out);
+    const size_t words = (size_t)E * (size_t)((T + 31) / 32);
+    if (words > kNoAllocWords)
+        return fail(MOEQ_ERR_SHAPE, "moe_permute_noalloc: E * ceil(T/32) = %zu exceeds its fixed scratch of %zu words",
+                    words, kNoAllocWords);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        cudaMemsetAsync(counts_out, 0, (size_t)E * 4, s);
+        cudaMemsetAsync(offsets_out, 0, (size_t)(E + 1) * 4, s);
+        if (int rc = cuda_check("moe_permute_noalloc")) return rc;
+        return ok();
+    }
+    REQ_PTR(idx);
+    REQ_PTR(perm_tok_out);
+    REQ_PTR(perm_slot_out);
+    REQ_PTR(inv_out);
+    unsigned *scratch = nullptr;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    // permute_kernel zeroes the bitmaps itself before use
+    permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, scratch, reinterpret_cast<int *>(scratch + kNoAllocWords),
+                                      counts_out, offsets_out, perm_tok_out, perm_slot_out, inv_out);
+    if (int rc = cuda_check("permute_kernel(noalloc)")) return rc;
     return ok();
 }
 
