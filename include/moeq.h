@@ -89,6 +89,11 @@ typedef struct moe_qweights {
  *            over the selected experts)
  * x [T,H] fp32, Wr [E,H] fp32, bias [E] fp32 or NULL; idx_out [T,k] int32,
  * w_out [T,k] fp32.  T = 0 is a no-op.
+ * For T <= 64 the router rows are fetched while the previous kernel on
+ * `stream` is still finishing (programmatic dependent launch), so Wr must be
+ * complete before the call is enqueued: do not write it from work that is
+ * still pending on `stream` (weights are written once, then synchronised).
+ * x and every other input are read only after earlier work has completed.
  */
 int moe_route_topk(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k,
                    int32_t *idx_out, float *w_out, void *ws, size_t ws_bytes, void *stream);
@@ -178,6 +183,10 @@ int moe_combine(const float *out_sorted, const int32_t *inv, const float *w, int
  * The whole layer: route + top-k, permutation, experts and combine, all on
  * `stream` with no host synchronisation.  y_out [T,H] = (residual ? x : 0) +
  * the routed mixture.  idx_out/w_out [T,k] optional (may be NULL).
+ * Decode calls (T <= 64 in GEMV mode) run as two kernels chained by
+ * programmatic dependent launch; the router weights Wr are fetched before the
+ * previous kernel on `stream` has finished (see moe_route_topk), so a stack
+ * of layers streams layer l+1's router while layer l's experts run.
  */
 int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias, const moe_qweights *weights,
                       int k, int residual, float *y_out, int32_t *idx_out, float *w_out, int mode, void *ws,

@@ -18,6 +18,23 @@ __device__ __forceinline__ void set_status(int bits) { atomicOr(&g_status, bits)
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 
+// One active expert's work record for the decode expert kernel: the expert,
+// the first sorted position of its (token, slot) pairs, their count, and the
+// first kUnitTok tokens with their routing weights (the rest are read from
+// the permutation arrays).
+constexpr int kUnitTok = 8;
+struct __align__(16) UnitRec {
+    int e, pb, ne, pad;
+    int tok[kUnitTok];
+    float w[kUnitTok];
+};
+
+// Byte position of element i of a 32-block in the order the 2-bit block dot
+// consumes activations: word m (m < 4) holds elements {m, 4+m, 8+m, 12+m},
+// word 4+m the same for elements 16..31 (what masking the packed 2-bit codes
+// with 0x03030303 after a shift by 2m lines up against).
+__host__ __device__ __forceinline__ int pack_pos2(int i) { return (4 * (i >> 4) + (i & 3)) * 4 + ((i & 15) >> 2); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -29,7 +29,7 @@
 // and returns.
 #pragma once
 
-#include "common.cuh"
+#include "async.cuh"
 #include "permute.cuh"
 
 namespace moeq {
@@ -69,54 +69,6 @@ struct GemmCfg {
 };
 
 // ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
-// Bounded wait for the phase with the given parity to complete.  Returns false
-// (and raises the CTA's abort flag) if it did not within the limit or if
-// another thread already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          bool honour_abort = true) {
-    if (mbar_try(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 15u) == 0u) {
-            if (honour_abort && *abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                set_status(MOEQ_STATUS_WAIT_TIMEOUT);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -238,7 +190,7 @@ __global__ void __launch_bounds__(256, 1) ffn_gemm_kernel(GemmArgs a) {
         }
         mbar_init(smem_u32(acc_bar), 1);
         *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_mbar_init();
     }
     if (warp == 4) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),

@@ -3,8 +3,12 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <string>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "combine.cuh"
 #include "common.cuh"
@@ -70,11 +74,13 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Token count up to which the routed experts run as GEMVs (auto mode).
 constexpr int kGemvMaxT = 64;
 // Token count up to which the decode fast path fuses routing and permutation.
-constexpr int kFusedRouteMaxT = kRouteTok;
+constexpr int kFusedRouteMaxT = kFusedMaxT;  // (the router kernel's tail handles up to 64 tokens)
+// Token count up to which every expert CTA ranks the router logits itself.
+constexpr int kInCtaRouteMaxT = 2;
 
 struct Layout {
-    size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, active, tiles, qx, sx,
-        ex, xhi, xlo, qh, sh, eh, hhi, hlo, total;
+    size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, units, tiles, qx, sx,
+        ex, xsum, xhi, xlo, qh, sh, eh, hhi, hlo, total;
 };
 
 Layout layout(long long T, long long H, long long I, long long E, long long k) {
@@ -98,11 +104,12 @@ Layout layout(long long T, long long H, long long I, long long E, long long k) {
     L.inv = take(P * 4);
     L.masks = take(E * W * 4);
     L.prefix = take(E * W * 4);
-    L.active = take(E * 4);
+    L.units = take(E * (long long)sizeof(UnitRec));
     L.tiles = take(max_tiles * (long long)sizeof(Tile));
     L.qx = take(T * H);
     L.sx = take(T * (H / 32) * 4);
     L.ex = take(T * 4);
+    L.xsum = take(T * (H / 32) * 4);
     L.xhi = take(T * H * 2);
     L.xlo = take(T * H * 2);
     L.qh = take(P * I);
@@ -176,51 +183,153 @@ void topk_dispatch(const float *logits, int T, int E, int k, int32_t *idx, float
     else launch_topk<32>(logits, T, E, k, idx, w, s);
 }
 
-template <int PER>
-void launch_route_gemv(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
-                       int fuse, const DecodeTail &tail, cudaStream_t s) {
-    const int blocks = (E + kRouteRows - 1) / kRouteRows;
-    route_gemv_kernel<PER><<<blocks, 256, 0, s>>>(x, T, H, Wr, bias, E, logits, fuse, tail);
+// Largest dynamic shared memory a CTA may opt into on this device.
+int max_smem_optin() {
+    static int v = 0;
+    if (!v) {
+        int dev = 0, val = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&val, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess && val > 0)
+            v = val;
+        else
+            v = 48 * 1024;
+    }
+    return v;
 }
 
-void route_gemv_dispatch(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
-                         int fuse, const DecodeTail &tail, cudaStream_t s) {
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous kernel on the stream finishes; it calls pdl_wait() before touching
+// anything that earlier work produces.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int PER>
+int launch_route_gemv(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
+                      const DecodeTail &tail, cudaStream_t s) {
+    const size_t smem = route_smem(H, E).total;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_gemv_kernel<PER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "route smem attribute: %s", cudaGetErrorString(e));
+    }
+    const unsigned blocks = (unsigned)((E + kRouteRows - 1) / kRouteRows);
+    cudaError_t e = launch_pdl(route_gemv_kernel<PER>, blocks, 256, smem, s, x, T, H, Wr, bias, E, logits, tail);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "route_gemv_kernel: %s", cudaGetErrorString(e));
+    return MOEQ_OK;
+}
+
+int route_gemv_dispatch(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
+                        const DecodeTail &tail, cudaStream_t s) {
     const int per = (E + 31) / 32;
-    if (per <= 1) launch_route_gemv<1>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
-    else if (per <= 2) launch_route_gemv<2>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
-    else if (per <= 4) launch_route_gemv<4>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
-    else if (per <= 8) launch_route_gemv<8>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
-    else if (per <= 16) launch_route_gemv<16>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
-    else launch_route_gemv<32>(x, T, H, Wr, bias, E, logits, fuse, tail, s);
+    if (per <= 1) return launch_route_gemv<1>(x, T, H, Wr, bias, E, logits, tail, s);
+    if (per <= 2) return launch_route_gemv<2>(x, T, H, Wr, bias, E, logits, tail, s);
+    if (per <= 4) return launch_route_gemv<4>(x, T, H, Wr, bias, E, logits, tail, s);
+    if (per <= 8) return launch_route_gemv<8>(x, T, H, Wr, bias, E, logits, tail, s);
+    if (per <= 16) return launch_route_gemv<16>(x, T, H, Wr, bias, E, logits, tail, s);
+    return launch_route_gemv<32>(x, T, H, Wr, bias, E, logits, tail, s);
 }
 
 // Router logits + top-k (unfused).
-void route_unfused(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k, int32_t *idx,
-                   float *w, float *logits, cudaStream_t s) {
+int route_unfused(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k, int32_t *idx,
+                  float *w, float *logits, cudaStream_t s) {
     if (T <= kGemvMaxT) {
         DecodeTail none{};
-        route_gemv_dispatch(x, T, H, Wr, bias, E, logits, 0, none, s);
+        if (int rc = route_gemv_dispatch(x, T, H, Wr, bias, E, logits, none, s)) return rc;
     } else {
         dim3 grid((E + kSgBN - 1) / kSgBN, (T + kSgBM - 1) / kSgBM);
         route_sgemm_kernel<<<grid, 256, 0, s>>>(x, T, H, Wr, bias, E, logits);
     }
     topk_dispatch(logits, T, E, k, idx, w, s);
+    return MOEQ_OK;
 }
 
-template <int BITS>
-int launch_gemv(const GemvArgs &g, int T, int k, int E, cudaStream_t s) {
-    const size_t smem = gemv_smem_bytes(g.H);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_gemv_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "gemv smem attribute: %s", cudaGetErrorString(e));
+// cuTensorMapEncodeTiled from the driver (looked up once, no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D TMA map over a row-major [rows][cols] array of esize-byte elements with
+// box {box_c, box_r}; no swizzle, zero fill outside the array.
+int tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint64_t esize, uint64_t cols, uint64_t rows,
+            uint32_t box_c, uint32_t box_r) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+    if (!enc) return fail(MOEQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * esize};
+    cuuint32_t box[2] = {box_c, box_r};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOEQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return MOEQ_OK;
+}
+
+template <int BITS, int PER>
+int launch_gemv(GemvArgs g, int T, int k, int E, cudaStream_t s) {
+    const int cap = max_smem_optin();
+    g.kc = std::min(g.H / 32, kGvMaxKB);
+    g.rc = std::min(g.H, kGvMaxRows);
+    g.tc = kGvTok;
+    auto need = [&]() { return (int)gemv_smem(g.H, BITS, g.kc, g.rc, g.tc).total; };
+    while (need() > cap && g.tc > 1) g.tc /= 2;
+    while (need() > cap && g.kc > 4) g.kc = (g.kc + 1) / 2;
+    while (need() > cap && g.rc > 128) g.rc /= 2;
+    const int smem = need();
+    if (smem > cap) return fail(MOEQ_ERR_SHAPE, "expert GEMV needs %d bytes of shared memory (%d available)", smem, cap);
+    if (g.route_mode == 1 && T > g.tc) return fail(MOEQ_ERR_SHAPE, "in-CTA routing needs T <= %d here", g.tc);
+    const uint64_t rows = (uint64_t)E * (uint64_t)(g.H / 32);  // (expert, K-block) rows of gate/up
+    for (int m = 0; m < 2; ++m) {
+        if (int rc = tmap_2d(&g.tm[m], g.codes[m], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)g.I * BITS, rows,
+                             32 * BITS, (uint32_t)g.kc))
+            return rc;
+        if (int rc = tmap_2d(&g.tm[2 + m], g.scales[m], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)g.I, rows, 32,
+                             (uint32_t)g.kc))
+            return rc;
     }
+    cudaError_t e = cudaFuncSetAttribute(ffn_gemv_kernel<BITS, PER>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "gemv smem attribute: %s", cudaGetErrorString(e));
     const long long units = std::min<long long>((long long)T * k, E);
     const long long blocks = units * (g.I / 32);
     if (blocks == 0) return MOEQ_OK;
     trace_begin(s);
-    ffn_gemv_kernel<BITS><<<(unsigned)blocks, 256, smem, s>>>(g);
+    e = launch_pdl(ffn_gemv_kernel<BITS, PER>, (unsigned)blocks, 256, (size_t)smem, s, g);
     trace_end(s);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "ffn_gemv_kernel: %s", cudaGetErrorString(e));
     return cuda_check("ffn_gemv_kernel");
+}
+
+int gemv_dispatch(const GemvArgs &g, int bits, int T, int k, int E, cudaStream_t s) {
+    const int per = (E + 31) / 32;
+#define MOEQ_GEMV(P_) return bits == 2 ? launch_gemv<2, P_>(g, T, k, E, s) : launch_gemv<3, P_>(g, T, k, E, s)
+    if (per <= 1) MOEQ_GEMV(1);
+    if (per <= 2) MOEQ_GEMV(2);
+    if (per <= 4) MOEQ_GEMV(4);
+    if (per <= 8) MOEQ_GEMV(8);
+    if (per <= 16) MOEQ_GEMV(16);
+    MOEQ_GEMV(32);
+#undef MOEQ_GEMV
 }
 
 template <bool GATEUP, int BITS>
@@ -238,11 +347,10 @@ int launch_gemm(const GemmArgs &g, long long max_tiles, cudaStream_t s) {
     return cuda_check("ffn_gemm_kernel");
 }
 
-// Experts over an existing permutation.  `plan_ready`: ctrl[1] / active were
-// already written by the fused decode routing.
+// Experts over an existing permutation.
 int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t *offsets, const int32_t *perm_tok,
             const int32_t *perm_slot, const float *w, float *out_sorted, float *y, int residual, int mode,
-            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, bool plan_ready, cudaStream_t s) {
+            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, cudaStream_t s) {
     const int H = wq->H, I = wq->I, E = wq->E, bits = wq->bits;
     const long long P = (long long)T * k;
     if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
@@ -253,13 +361,19 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
         if (blocks > 0) init_y_kernel<<<blocks, 256, 0, s>>>(x, y, n, residual);
     }
     if (T == 0) return cuda_check("init_y_kernel");
-    if (!plan_ready)
-        plan_kernel<<<1, 1024, 0, s>>>(offsets, E, ctrl, at<int32_t>(ws, L.active), at<Tile>(ws, L.tiles));
+    plan_kernel<<<1, 1024, 0, s>>>(offsets, E, ctrl, mode == MOEQ_MODE_GEMV ? at<UnitRec>(ws, L.units) : nullptr,
+                                   perm_tok, perm_slot, y ? w : nullptr, k, at<Tile>(ws, L.tiles));
     if (int rc = cuda_check("plan_kernel")) return rc;
     if (mode == MOEQ_MODE_GEMV) {
         if (out_sorted) cudaMemsetAsync(out_sorted, 0, (size_t)P * H * sizeof(float), s);
+        quant_rows_kernel<<<T, 256, 0, s>>>(x, H, at<int8_t>(ws, L.qx), at<float>(ws, L.sx), nullptr, nullptr,
+                                            nullptr, nullptr, nullptr, nullptr, at<int>(ws, L.xsum), bits == 2);
+        if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
         GemvArgs g{};
         g.x = x;
+        g.qx = at<int8_t>(ws, L.qx);
+        g.sx = at<float>(ws, L.sx);
+        g.xsum = at<int>(ws, L.xsum);
         g.T = T;
         g.H = H;
         g.I = I;
@@ -269,17 +383,17 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
             g.codes[m] = wq->codes[m];
             g.scales[m] = wq->scales[m];
         }
-        g.offsets = offsets;
         g.perm_tok = perm_tok;
         g.perm_slot = perm_slot;
         g.w = w;
-        g.active = at<int32_t>(ws, L.active);
+        g.units = at<UnitRec>(ws, L.units);
         g.ctrl = ctrl;
+        g.route_mode = 0;
         g.y = y;
         g.out_sorted = out_sorted;
         g.qh_out = qh_out;
         g.sh_out = sh_out;
-        return bits == 2 ? launch_gemv<2>(g, T, k, E, s) : launch_gemv<3>(g, T, k, E, s);
+        return gemv_dispatch(g, bits, T, k, E, s);
     }
     // grouped tensor-core GEMMs
     int8_t *qx = at<int8_t>(ws, L.qx);
@@ -290,7 +404,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     float *sh = sh_out ? sh_out : at<float>(ws, L.sh);
     int *eh = at<int>(ws, L.eh);
     __half *hhi = at<__half>(ws, L.hhi), *hlo = at<__half>(ws, L.hlo);
-    quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, xhi, xlo, ex, nullptr, nullptr, nullptr);
+    quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, xhi, xlo, ex, nullptr, nullptr, nullptr, nullptr, 0);
     if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
     const long long max_tiles = (P + kTileN - 1) / kTileN + E;
     GemmArgs g{};
@@ -315,7 +429,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     g.sh = sh;
     int rc = bits == 2 ? launch_gemm<true, 2>(g, max_tiles, s) : launch_gemm<true, 3>(g, max_tiles, s);
     if (rc) return rc;
-    quant_rows_kernel<<<(unsigned)P, 256, 0, s>>>(nullptr, I, nullptr, nullptr, hhi, hlo, eh, qh, sh, nullptr);
+    quant_rows_kernel<<<(unsigned)P, 256, 0, s>>>(nullptr, I, nullptr, nullptr, hhi, hlo, eh, qh, sh, nullptr, nullptr, 0);
     if ((rc = cuda_check("quant_rows_kernel(h)"))) return rc;
     g.bhi = hhi;
     g.blo = hlo;
@@ -389,7 +503,7 @@ int moe_route_topk(const float *x, int T, int H, const float *Wr, const float *b
     if (!ws || !aligned(ws, 256)) return fail(MOEQ_ERR_ALIGN, "ws missing or not 256-byte aligned");
     if (T == 0) return ok();
     cudaStream_t s = (cudaStream_t)stream;
-    route_unfused(x, T, H, Wr, bias, E, k, idx_out, w_out, at<float>(ws, L.logits), s);
+    if (int rc = route_unfused(x, T, H, Wr, bias, E, k, idx_out, w_out, at<float>(ws, L.logits), s)) return rc;
     if (int rc = cuda_check("moe_route_topk")) return rc;
     return ok();
 }
@@ -457,7 +571,7 @@ int moe_quantize_act(const float *x, int T, int H, int8_t *q_out, float *s_out, 
     REQ_PTR(q_out);
     REQ_PTR(s_out);
     quant_rows_kernel<<<T, 256, 0, (cudaStream_t)stream>>>(x, H, q_out, s_out, nullptr, nullptr, nullptr, nullptr,
-                                                            nullptr, nullptr);
+                                                            nullptr, nullptr, nullptr, 0);
     if (int rc = cuda_check("quant_rows_kernel")) return rc;
     return ok();
 }
@@ -486,7 +600,7 @@ int moe_expert_ffn_q2(const float *x, int T, const moe_qweights *weights, int k,
     const Layout L = layout(T, H, I, E, k);
     if (int rc = check_ws(ws, ws_bytes, L)) return rc;
     if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, out_sorted, y, residual, mode, qh_out,
-                         sh_out, ws, L, false, (cudaStream_t)stream))
+                         sh_out, ws, L, (cudaStream_t)stream))
         return rc;
     return ok();
 }
@@ -533,13 +647,35 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
     int32_t *inv = at<int32_t>(ws, L.inv);
     if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
     if (T <= kFusedRouteMaxT && mode == MOEQ_MODE_GEMV) {
-        // decode: router + top-k + permutation + y init in one kernel, then the experts
-        DecodeTail tail{k, idx, w, counts, offsets, perm_tok, perm_slot, inv, at<int32_t>(ws, L.active),
-                        at<int>(ws, L.ctrl), y_out, residual};
-        route_gemv_dispatch(x, T, H, Wr, bias, E, at<float>(ws, L.logits), 1, tail, s);
-        if (int rc = cuda_check("route_gemv_kernel(fused)")) return rc;
+        // decode: two kernels chained by programmatic dependent launch.  The
+        // router kernel also sets y = residual ? x : 0 and quantises x.  For
+        // T <= kInCtaRouteMaxT every expert CTA ranks the logits itself (one
+        // warp per token, no separate routing step); above that the router's
+        // last CTA groups the pairs into per-expert records once.
+        const bool in_cta = T <= kInCtaRouteMaxT;
+        DecodeTail tail{};
+        tail.mode = in_cta ? 1 : 2;
+        tail.k = k;
+        tail.idx = idx;
+        tail.w = w;
+        tail.perm_tok = perm_tok;
+        tail.perm_slot = perm_slot;
+        tail.inv = inv;
+        tail.units = at<UnitRec>(ws, L.units);
+        tail.ctrl = at<int>(ws, L.ctrl);
+        tail.y = y_out;
+        tail.residual = residual;
+        tail.qx = at<int8_t>(ws, L.qx);
+        tail.sx = at<float>(ws, L.sx);
+        tail.xsum = at<int>(ws, L.xsum);
+        tail.bits = weights->bits;
+        float *logits = at<float>(ws, L.logits);
+        if (int rc = route_gemv_dispatch(x, T, H, Wr, bias, E, logits, tail, s)) return rc;
         GemvArgs g{};
         g.x = x;
+        g.qx = tail.qx;
+        g.sx = tail.sx;
+        g.xsum = tail.xsum;
         g.T = T;
         g.H = H;
         g.I = I;
@@ -549,24 +685,26 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
             g.codes[m] = weights->codes[m];
             g.scales[m] = weights->scales[m];
         }
-        g.offsets = offsets;
         g.perm_tok = perm_tok;
         g.perm_slot = perm_slot;
         g.w = w;
-        g.active = at<int32_t>(ws, L.active);
-        g.ctrl = at<int>(ws, L.ctrl);
+        g.units = tail.units;
+        g.ctrl = tail.ctrl;
+        g.route_mode = in_cta ? 1 : 0;
+        g.logits = logits;
+        g.idx_out = idx_out;
+        g.w_out = w_out;
         g.y = y_out;
-        int rc = weights->bits == 2 ? launch_gemv<2>(g, T, k, E, s) : launch_gemv<3>(g, T, k, E, s);
-        if (rc) return rc;
+        if (int rc = gemv_dispatch(g, weights->bits, T, k, E, s)) return rc;
         return ok();
     }
-    route_unfused(x, T, H, Wr, bias, E, k, idx, w, at<float>(ws, L.logits), s);
+    if (int rc = route_unfused(x, T, H, Wr, bias, E, k, idx, w, at<float>(ws, L.logits), s)) return rc;
     if (int rc = cuda_check("route")) return rc;
     permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, at<unsigned>(ws, L.masks), at<int>(ws, L.prefix), counts, offsets,
                                       perm_tok, perm_slot, inv);
     if (int rc = cuda_check("permute_kernel")) return rc;
     if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, nullptr, y_out, residual, mode, nullptr,
-                         nullptr, ws, L, false, s))
+                         nullptr, ws, L, s))
         return rc;
     return ok();
 }

@@ -62,8 +62,10 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict
     }
 }
 
-// Work plan from offsets: the list of experts with at least one pair, and the
-// list of (expert, first sorted position, rows) tiles of up to kTileN pairs.
+// Work plan from offsets: the number of experts with at least one pair and
+// their UnitRec records (for the decode expert kernel; units may be NULL), and
+// the list of (expert, first sorted position, rows) tiles of up to kTileN
+// pairs (for the tensor-core kernels).
 constexpr int kTileN = 128;
 
 struct Tile {
@@ -71,7 +73,9 @@ struct Tile {
 };
 
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int E, int *ctrl,
-                                                    int32_t *active, Tile *tiles) {
+                                                    UnitRec *units, const int32_t *__restrict__ perm_tok,
+                                                    const int32_t *__restrict__ perm_slot,
+                                                    const float *__restrict__ w, int k, Tile *tiles) {
     __shared__ int s_act[kMaxE];
     __shared__ int s_til[kMaxE];
     __shared__ int s_scan[33];
@@ -86,7 +90,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     const int n_tiles = block_exclusive_scan(s_til, E, s_scan);
     for (int e = tid; e < E; e += blockDim.x) {
         const int o = offsets[e], c = offsets[e + 1] - o;
-        if (c > 0) active[s_act[e]] = e;
+        if (c > 0 && units) {
+            UnitRec *r = units + s_act[e];
+            *reinterpret_cast<int4 *>(r) = make_int4(e, o, c, 0);
+            for (int i = 0; i < min(c, kUnitTok); ++i) {
+                const int t = perm_tok[o + i];
+                r->tok[i] = t;
+                r->w[i] = w ? w[(size_t)t * k + perm_slot[o + i]] : 0.f;
+            }
+        }
         for (int i = 0; i * kTileN < c; ++i) {
             Tile tl;
             tl.e = e;

@@ -10,13 +10,16 @@ namespace moeq {
 
 // One CTA (256 threads) per row of n values (n multiple of 32).  Warp w
 // quantises blocks w, w+8, ...; lane i holds element i of the block.
-// Optional outputs: hi/lo fp16 rows of q*s*2^-e with e = row_exponent(max s).
+// Optional outputs: hi/lo fp16 rows of q*s*2^-e with e = row_exponent(max s);
+// sum_out[row][b] = the sum of the block's codes.  pack2: q is stored in the
+// 2-bit block dot's order (pack_pos2) instead of the natural order (no hi/lo).
 // `src_q`/`src_s` non-null: the row is already quantised (only the split runs).
 __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict__ v, int n, int8_t *q_out,
                                                          float *s_out, __half *hi, __half *lo, int *e_out,
                                                          const int8_t *__restrict__ src_q,
                                                          const float *__restrict__ src_s,
-                                                         const int32_t *__restrict__ row_map) {
+                                                         const int32_t *__restrict__ row_map,
+                                                         int *sum_out, int pack2) {
     const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nb = n / 32;
@@ -36,7 +39,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict
         for (int b = warp; b < nb; b += 8) {
             const float val = vr[32 * b + lane];
             const float s = block_scale(warp_absmax(val));
-            qr[32 * b + lane] = (int8_t)block_code(val, s);
+            const int q = block_code(val, s);
+            qr[32 * b + (pack2 ? pack_pos2(lane) : lane)] = (int8_t)q;
+            if (sum_out) {
+                const int qs = warp_sum_int(q);
+                if (lane == 0) sum_out[(size_t)row * nb + b] = qs;
+            }
             if (lane == 0) sr[b] = s;
             smax = fmaxf(smax, s);
         }

@@ -48,6 +48,7 @@ class LayerCase:
         self.layer = synth.make_layer(shape, seed=seed, device=device, skew=skew)
         self.np = self.layer.numpy()
         self.dev = self.layer.to(_dev())
+        torch.cuda.synchronize()  # weights complete before any call reads them
         import quantized_mixture_experts_token_b300 as moeq
 
         self.W = moeq.ExpertWeights.from_layer(self.dev)
