@@ -14,20 +14,16 @@
 //     epilogue per K-block;
 //   * e is a per-row power of two, undone exactly in the epilogue.
 //
-// Kernel shape (one CTA per (128-row M tile, <=128-token N tile), 8 warps):
-//   warps 0-3  producers: cp.async the raw 2-bit codes / fp16 scales of the A
-//              tile and the gathered B rows into a 3-4 stage ring, then unpack
-//              the codes into the 128B-swizzled K-major fp16 A tile;
-//   warp 4     allocates TMEM and issues tcgen05.mma from one thread;
-//   warps 4-7  epilogue: tcgen05.ld the accumulator (lane = M row), then
-//              gate/up: h = silu(G) * U and int8 re-quantisation per 32 rows
-//                       (one warp = one quantisation block), stored as q_h, s_h;
-//              down:    D * 2^e, weighted by the routing weight and added into
-//                       y (red.add), or stored per sorted pair.
-// Every mbarrier wait is bounded; a wait that gives up records
-// MOEQ_STATUS_WAIT_TIMEOUT, the CTA drains its copies and MMAs, frees TMEM
-// and returns.
+// Work item = (tile of <= 128 sorted pairs of one expert, 128-row block of its
+// weight matrix); the epilogue reads the accumulator (lane = weight row):
+//   gate/up: h = silu(G) * U and int8 re-quantisation per 32 rows (one warp =
+//            one quantisation block), stored as q_h, s_h;
+//   down:    D * 2^e, weighted by the routing weight and added into y
+//            (fp32 atomics), or stored per sorted pair.
+// The kernel is persistent and warp-specialised (see ffn_gemm_kernel).
 #pragma once
+
+#include <cuda.h>
 
 #include "async.cuh"
 #include "permute.cuh"
@@ -46,45 +42,17 @@ struct GemmArgs {
     const int *ctrl;  // ctrl[2] = number of tiles
     const int32_t *perm_tok, *perm_slot;
     const float *w;
-    const __half *bhi, *blo;  // B rows: x by token (gate/up) or h by sorted position (down)
-    const int *brow_exp;      // their power-of-two exponents
+    const __half *bhi, *blo;  // B rows by sorted pair position: x of the pair's token (gate/up) or h (down)
+    const int *brow_exp;      // their power-of-two exponents, per sorted pair
     int8_t *qh;               // gate/up outputs [T*k, I]
     float *sh;                // [T*k, I/32]
     float *y, *out_sorted;    // down outputs
-};
-
-template <bool GATEUP, int BITS>
-struct GemmCfg {
-    static constexpr int NA = GATEUP ? 2 : 1;
-    static constexpr int STAGES = GATEUP ? 3 : 4;
-    static constexpr int BPB = 4 * BITS;
-    static constexpr int A_BYTES = kGmM * kGmK * 2;  // 16 KB
-    static constexpr int B_BYTES = kGmN * kGmK * 2;  // 16 KB (hi or lo)
-    static constexpr int TILE_BYTES = NA * A_BYTES + 2 * B_BYTES;
-    static constexpr int RAW_CODES = NA * 2 * kGmM * BPB;  // 2 K-blocks per stage
-    static constexpr int RAW_SCALES = NA * 2 * kGmM * 2;
-    static constexpr int RAW_BYTES = RAW_CODES + RAW_SCALES;
-    static constexpr int TMEM_COLS = 256;
-    static constexpr size_t SMEM = 1024 /*align slack*/ + (size_t)STAGES * (TILE_BYTES + RAW_BYTES) + 2048;
+    // TMA maps of the B rows (fp16 [P][K], 128-byte swizzle): [0] hi, [1] lo with
+    // 64 x 16-row boxes, [2] hi, [3] lo with 64 x 128-row boxes
+    CUtensorMap bmap[4];
 };
 
 // ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -154,137 +122,264 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lo, uint32_t lut_hi, u
 // ------------------------------------------------------------------ kernel
 
 template <bool GATEUP, int BITS>
-__global__ void __launch_bounds__(256, 1) ffn_gemm_kernel(GemmArgs a) {
+struct GemmCfg {
+    static constexpr int NA = GATEUP ? 2 : 1;  // weight matrices per work item (gate + up, or down)
+    static constexpr int BPB = 4 * BITS;
+    static constexpr int STAGES = GATEUP ? 3 : 4;                  // operand ring, K = 64 per stage
+    static constexpr int RSTAGES = (GATEUP && BITS == 3) ? 4 : 6;  // raw-code ring (runs further ahead)
+    static constexpr int A_BYTES = kGmM * kGmK * 2;                // fp16 weight tile
+    static constexpr int B_BYTES = kGmN * kGmK * 2;                // fp16 activation tile (hi or lo)
+    static constexpr int SLOT_BYTES = NA * A_BYTES + 2 * B_BYTES;
+    static constexpr int RAW_CODES = NA * 2 * kGmM * BPB;  // two K-blocks per stage
+    static constexpr int RAW_SCALES = NA * 2 * kGmM * 2;
+    static constexpr int RAW_BYTES = RAW_CODES + RAW_SCALES;
+    static constexpr int ACC_COLS = NA * kGmN;      // one accumulator buffer (fp32 columns)
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;  // double buffered: 512 (gate/up) or 256 (down)
+    static constexpr int NUM_BARS = 2 * RSTAGES + 3 * STAGES + 5;
+    static constexpr int MISC_BYTES = 8 * NUM_BARS + 16 + 3 * 2 * kGmN * 4;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES;
+    static constexpr int THREADS = 320;  // 10 warps, see the kernel
+};
+
+// Four rows (r0..r3) of 64 fp16 starting at column x of a 2-D tensor map with a
+// one-row box, into 4 consecutive 128-byte rows of shared memory (swizzled by
+// the map).  Completes on `bar` (512 bytes).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Persistent grouped GEMM: one CTA per SM walks the work items q = blockIdx.x,
+// blockIdx.x + gridDim.x, ... where q = (tile, 128-row M block).  Each item is
+// K/64 pipeline stages; stage g of this CTA uses operand slot g % STAGES and
+// raw slot g % RSTAGES, so every role derives the same slot and phase from g.
+//   warp 0     producer: bulk copies of the raw codes/scales (RSTAGES ahead)
+//              and 2-D TMA loads of the tile's B rows (hi, lo; contiguous in
+//              sorted pair order) into the swizzled slots, on mbarriers
+//   warp 1     TMEM owner; lane 0 issues the MMAs (hi and lo per K step)
+//   warps 2-5  unpack: row r of the weight tile, codes -> fp16 level*scale
+//   warps 6-9  epilogue on the other accumulator buffer (TMEM lane quadrant
+//              = warp % 4), so item i's epilogue overlaps item i+1's MMAs
+// Every wait is bounded; a wait that gives up raises the CTA's abort flag,
+// every role leaves its loop, copies and MMAs are drained and TMEM is freed.
+template <bool GATEUP, int BITS>
+__global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant__ GemmArgs a) {
     using C = GemmCfg<GATEUP, BITS>;
+    constexpr int NA = C::NA, BPB = C::BPB, S = C::STAGES, R = C::RSTAGES;
     const int MT = (GATEUP ? a.I : a.H) / kGmM;
-    const int tile_idx = blockIdx.x / MT, mt = blockIdx.x % MT;
-    if (tile_idx >= a.ctrl[2]) return;
-    const Tile tile = a.tiles[tile_idx];
-    const int e = tile.e, p0 = tile.p0, nval = tile.n;
-    const int nround = (nval + 15) & ~15;
     const int K = GATEUP ? a.H : a.I;
     const int KB = K / 32, nk = K / kGmK;
-    const int NR = GATEUP ? a.I : a.H;  // rows of each A matrix
-    const int m0 = mt * kGmM;
+    const int NR = GATEUP ? a.I : a.H;  // rows of each weight matrix
+    const int n_items = a.ctrl[2] * MT;
+    const int nq = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int G = nq * nk;  // pipeline stages of this CTA
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *tiles_base = smem;                                    // STAGES x TILE_BYTES
-    unsigned char *raw_base = smem + (size_t)C::STAGES * C::TILE_BYTES;  // STAGES x RAW_BYTES
-    unsigned char *misc = raw_base + (size_t)C::STAGES * C::RAW_BYTES;
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc);
-    uint64_t *empty_bar = full_bar + C::STAGES;
-    uint64_t *acc_bar = empty_bar + C::STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
+    unsigned char *slots = smem;                                       // S x SLOT_BYTES
+    unsigned char *raws = smem + (size_t)S * C::SLOT_BYTES;            // R x RAW_BYTES
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raws + (size_t)R * C::RAW_BYTES);
+    uint64_t *raw_full = bars, *raw_empty = bars + R;
+    uint64_t *a_full = bars + 2 * R, *b_full = a_full + S, *slot_empty = b_full + S;
+    uint64_t *acc_full = slot_empty + S, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *s_exp = reinterpret_cast<int *>(misc + 256);    // [kGmN] B-row exponents
-    int *s_tok = s_exp + kGmN;                            // [kGmN] token of each B row
-    float *s_wt = reinterpret_cast<float *>(s_tok + kGmN);  // [kGmN] routing weight of each row
+    int *s_tok = reinterpret_cast<int *>(tmem_slot + 4);  // [2][kGmN] per accumulator buffer
+    int *s_exp = s_tok + 2 * kGmN;
+    float *s_wt = reinterpret_cast<float *>(s_exp + 2 * kGmN);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
     if (tid == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 128);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+        for (int i = 0; i < R; ++i) {
+            mbar_init(smem_u32(&raw_full[i]), 1);
+            mbar_init(smem_u32(&raw_empty[i]), 128);
         }
-        mbar_init(smem_u32(acc_bar), 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&a_full[i]), 128);
+            mbar_init(smem_u32(&b_full[i]), 1);
+            mbar_init(smem_u32(&slot_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&acc_full[i]), 1);
+            mbar_init(smem_u32(&acc_empty[i]), 128);
+        }
+        mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(C::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (tid < kGmN) {
-        const int j = min(tid, nval - 1);
-        const int p = p0 + j;
-        const int t = a.perm_tok[p];
-        s_tok[tid] = t;
-        s_exp[tid] = a.brow_exp[GATEUP ? t : p];
-        s_wt[tid] = (!GATEUP && a.w) ? a.w[(size_t)t * a.k + a.perm_slot[p]] : 0.f;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
-        // ------------------------------------------------------ producers
-        const int r = tid;  // A row of this thread
-        const uint8_t *cptr[2];
-        const uint16_t *sptr[2];
-#pragma unroll
-        for (int m = 0; m < C::NA; ++m) {
-            const int mat = GATEUP ? m : 2;
-            cptr[m] = a.codes[mat] + ((size_t)e * KB * NR + m0 + r) * C::BPB;
-            sptr[m] = a.scales[mat] + (size_t)e * KB * NR + m0 + (r & ~1);
-        }
-        // B rows this thread copies: chunk c, rows rb + 16 i
-        const int bc = tid & 7, rb = tid >> 3;
-        auto issue = [&](int ks) {
-            const int s = ks % C::STAGES;
-            unsigned char *tb = tiles_base + (size_t)s * C::TILE_BYTES;
-            unsigned char *rw = raw_base + (size_t)s * C::RAW_BYTES;
-            const uint32_t bhi_s = smem_u32(tb + C::NA * C::A_BYTES);
-            const uint32_t blo_s = bhi_s + C::B_BYTES;
-            const int k0 = ks * kGmK;
-            for (int i = 0; i < 8; ++i) {
-                const int row = rb + 16 * i;
-                if (row >= nround) break;
-                const int src_row = GATEUP ? s_tok[row] : p0 + min(row, nval - 1);
-                const size_t off = (size_t)src_row * K + k0 + 8 * bc;
-                const uint32_t so = sw128_off(row, bc);
-                cp_async_16(bhi_s + so, a.bhi + off);
-                cp_async_16(blo_s + so, a.blo + off);
-            }
-#pragma unroll
-            for (int m = 0; m < C::NA; ++m)
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int kb = 2 * ks + b;
-                    const uint32_t cdst = smem_u32(rw + ((m * 2 + b) * kGmM + r) * C::BPB);
-                    const uint8_t *csrc = cptr[m] + (size_t)kb * NR * C::BPB;
-                    if (BITS == 2) {
-                        cp_async_8(cdst, csrc);
-                    } else {
-                        cp_async_4(cdst, csrc);
-                        cp_async_4(cdst + 4, csrc + 4);
-                        cp_async_4(cdst + 8, csrc + 8);
-                    }
-                    const uint32_t sdst = smem_u32(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + (r & ~1)) * 2);
-                    cp_async_4(sdst, sptr[m] + (size_t)kb * NR);
-                }
-        };
-        // prologue: steps 0 .. STAGES-2 in flight
-        for (int ks = 0; ks < C::STAGES - 1; ++ks) {
-            if (ks < nk) issue(ks);
-            cp_async_commit();
-        }
+    // work item j of this CTA -> (tile, first weight row)
+    auto item = [&](int j, Tile &tl, int &m0) {
+        const int q = (int)blockIdx.x + j * (int)gridDim.x;
+        tl = a.tiles[q / MT];
+        m0 = (q % MT) * kGmM;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane < 4) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.bmap[lane])) : "memory");
+        const uint64_t pol = l2_evict_first();
+        int graw = 0, raw_j = -1, raw_m0 = 0;
+        Tile raw_tl{};
+        int b_j = -1;
+        Tile b_tl{};
+        int gb = 0;                 // B stages issued
         bool ok = true;
-        for (int ks = 0; ks < nk && ok; ++ks) {
-            const int s = ks % C::STAGES;
-            cp_async_wait<C::STAGES - 2>();  // this thread's copies of step ks have landed
-            __syncwarp();                    // ... and those of the lane sharing its scale word
-            unsigned char *tb = tiles_base + (size_t)s * C::TILE_BYTES;
-            const unsigned char *rw = raw_base + (size_t)s * C::RAW_BYTES;
+        for (int g = 0; g < G && ok; ++g) {
+            // raw codes/scales, up to R stages ahead of the operands
+            for (; graw < G && graw < g + R; ++graw) {
+                const int j = graw / nk, ks = graw - j * nk;
+                if (j != raw_j) {
+                    item(j, raw_tl, raw_m0);
+                    raw_j = j;
+                }
+                const int rs = graw % R;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&raw_empty[rs]), ((graw / R) & 1) ^ 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rbar = smem_u32(&raw_full[rs]);
+                if (lane == 0) mbar_arrive_expect_tx(rbar, (uint32_t)C::RAW_BYTES);
+                __syncwarp();
+                if (lane < 4 * NA) {  // lanes [0, 2NA): codes of (matrix, block); [2NA, 4NA): scales
+                    const int mb = lane % (2 * NA), m = mb >> 1, kb = 2 * ks + (mb & 1);
+                    const int mat = GATEUP ? m : 2;
+                    const size_t blk = ((size_t)raw_tl.e * KB + kb) * NR + raw_m0;
+                    unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
+                    if (lane < 2 * NA)
+                        bulk_g2s(smem_u32(rw + mb * kGmM * BPB), a.codes[mat] + blk * BPB, kGmM * BPB, rbar, pol);
+                    else
+                        bulk_g2s(smem_u32(rw + C::RAW_CODES + mb * kGmM * 2), a.scales[mat] + blk, kGmM * 2, rbar, pol);
+                }
+            }
+            if (!ok) break;
+            // B rows of stage g: activations hi/lo of sorted pairs p0 .. p0 + nround,
+            // K columns [64 ks, 64 ks + 64): one 128-row box per half for a full
+            // tile, else one 16-row box per 16 rows (lane i: rows 16 i ..)
+            const int j = g / nk, ks = g - j * nk;
+            if (j != b_j) {
+                int m0u;
+                item(j, b_tl, m0u);
+                b_j = j;
+            }
+            const int s = g % S;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&slot_empty[s]), ((g / S) & 1) ^ 1, abort_flag))) {
+                ok = false;
+                break;
+            }
+            const int nround = (b_tl.n + 15) & ~15;
+            const uint32_t bbar = smem_u32(&b_full[s]);
+            const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + NA * C::A_BYTES), blo = bhi + C::B_BYTES;
+            if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(2 * nround * kGmK * 2));
+            __syncwarp();
+            if (nround == kGmN) {
+                if (lane < 2) tma_load_2d(lane ? blo : bhi, &a.bmap[2 + lane], ks * kGmK, b_tl.p0, bbar, 0);
+            } else if (16 * lane < nround) {
+                tma_load_2d(bhi + 2048 * lane, &a.bmap[0], ks * kGmK, b_tl.p0 + 16 * lane, bbar, 0);
+                tma_load_2d(blo + 2048 * lane, &a.bmap[1], ks * kGmK, b_tl.p0 + 16 * lane, bbar, 0);
+            }
+            gb = g + 1;
+        }
+        if (!ok && lane == 0) {  // drain the copies still in flight
+            for (int g2 = max(0, graw - R); g2 < graw; ++g2)
+                mbar_wait(smem_u32(&raw_full[g2 % R]), (g2 / R) & 1, abort_flag, false);
+            for (int g2 = max(0, gb - S); g2 < gb; ++g2)
+                mbar_wait(smem_u32(&b_full[g2 % S]), (g2 / S) & 1, abort_flag, false);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int cur_j = -1;
+            uint32_t idesc = 0;
+            for (int g = 0; g < G; ++g) {
+                const int j = g / nk, ks = g - j * nk, buf = j & 1;
+                if (j != cur_j) {
+                    Tile tl;
+                    int m0;
+                    item(j, tl, m0);
+                    idesc = f16_idesc(kGmM, (tl.n + 15) & ~15);
+                    cur_j = j;
+                }
+                if (ks == 0) {
+                    if (!mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag)) break;
+                    tc_fence_after();
+                }
+                const int s = g % S;
+                const uint32_t ph = (g / S) & 1;
+                if (!mbar_wait(smem_u32(&a_full[s]), ph, abort_flag)) break;
+                if (!mbar_wait(smem_u32(&b_full[s]), ph, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t sb = smem_u32(slots + (size_t)s * C::SLOT_BYTES);
+                const uint32_t bhi = sb + NA * C::A_BYTES, blo = bhi + C::B_BYTES;
 #pragma unroll
-            for (int m = 0; m < C::NA; ++m) {
-                const uint32_t at = smem_u32(tb + m * C::A_BYTES);
+                for (int kk = 0; kk < kGmK / 16; ++kk) {
+                    const uint64_t bh = sw128_desc(bhi + 32 * kk), bl = sw128_desc(blo + 32 * kk);
+#pragma unroll
+                    for (int m = 0; m < NA; ++m) {
+                        const uint64_t ad = sw128_desc(sb + m * C::A_BYTES + 32 * kk);
+                        const uint32_t acc = tmem + (uint32_t)(buf * C::ACC_COLS + m * kGmN);
+                        mma_f16(acc, ad, bh, idesc, (ks | kk) != 0);
+                        mma_f16(acc, ad, bl, idesc, 1u);
+                    }
+                }
+                mma_commit(smem_u32(&slot_empty[s]));
+                if (ks == nk - 1) mma_commit(smem_u32(&acc_full[buf]));
+            }
+            // every MMA issued above is complete once this commit lands
+            mma_commit(smem_u32(drain));
+            mbar_wait(smem_u32(drain), 0, abort_flag, false);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ----------------------------------------------------------- unpack
+        const int r = tid - 64;  // weight row of the tile
+        for (int g = 0; g < G; ++g) {
+            const int rs = g % R;
+            if (!mbar_wait(smem_u32(&raw_full[rs]), (g / R) & 1, abort_flag)) break;
+            const unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
+            uint32_t cw[NA][2][BITS];
+            uint16_t sbits[NA][2];
+#pragma unroll
+            for (int m = 0; m < NA; ++m)
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
-                    const uint16_t sbits = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + r) * 2);
-                    const __half sc = __ushort_as_half(sbits);
+                    const uint32_t *cp = reinterpret_cast<const uint32_t *>(rw + ((m * 2 + b) * kGmM + r) * BPB);
+#pragma unroll
+                    for (int i = 0; i < BITS; ++i) cw[m][b][i] = cp[i];
+                    sbits[m][b] = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + r) * 2);
+                }
+            mbar_arrive(smem_u32(&raw_empty[rs]));
+            const int s = g % S;
+            if (!mbar_wait(smem_u32(&slot_empty[s]), ((g / S) & 1) ^ 1, abort_flag)) break;
+            unsigned char *sb = slots + (size_t)s * C::SLOT_BYTES;
+#pragma unroll
+            for (int m = 0; m < NA; ++m) {
+                const uint32_t at = smem_u32(sb + m * C::A_BYTES);
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const __half sc = __ushort_as_half(sbits[m][b]);
                     if (BITS == 2) {
-                        const uint2 cw = *reinterpret_cast<const uint2 *>(rw + ((m * 2 + b) * kGmM + r) * C::BPB);
                         const __half m2 = __hmul(sc, __float2half(-2.0f)), m1 = __hneg(sc);
                         const uint32_t lut_lo = (uint32_t)__half_as_ushort(m2) | ((uint32_t)__half_as_ushort(m1) << 16);
                         const uint32_t lut_hi = (uint32_t)__half_as_ushort(sc) << 16;  // {0, s}
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 8 elements = 2 code bytes
-                            const uint32_t word = c < 2 ? cw.x : cw.y;
+                            const uint32_t word = cw[m][b][c >> 1];
                             const uint32_t d0 = (word >> (16 * (c & 1))) & 0xffu;
                             const uint32_t d1 = (word >> (16 * (c & 1) + 8)) & 0xffu;
                             const uint32_t q0 = lut_pair(lut_lo, lut_hi, (d0 & 3u) | ((d0 & 0xCu) << 6));
@@ -294,126 +389,98 @@ __global__ void __launch_bounds__(256, 1) ffn_gemm_kernel(GemmArgs a) {
                             st_shared_v4(at + sw128_off(r, 4 * b + c), q0, q1, q2, q3);
                         }
                     } else {
-                        // 3-bit levels -4..3 times s: +-3s need not be exact in fp16 (documented;
-                        // the GEMV path is exact for 3-bit)
-                        const uint32_t *cw = reinterpret_cast<const uint32_t *>(rw + ((m * 2 + b) * kGmM + r) * C::BPB);
-                        const uint32_t w0 = cw[0], w1 = cw[1], w2 = cw[2];
+                        // 3-bit levels -4..3 times s: +-3s need not be exact in fp16 (the GEMV path is exact)
                         const float sf = __half2float(sc);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            uint32_t q[4];
+                            uint32_t qv[4];
 #pragma unroll
                             for (int h2 = 0; h2 < 4; ++h2) {
                                 __half hv[2];
 #pragma unroll
                                 for (int u = 0; u < 2; ++u) {
                                     const int i = 8 * c + 2 * h2 + u, off = 3 * i, wi = off >> 5, sh = off & 31;
-                                    const uint32_t lo = wi == 0 ? w0 : (wi == 1 ? w1 : w2);
-                                    const uint32_t hi = wi == 0 ? w1 : (wi == 1 ? w2 : 0u);
+                                    const uint32_t lo = cw[m][b][wi];
+                                    const uint32_t hi = wi + 1 < BITS ? cw[m][b][wi + 1] : 0u;
                                     const int code = (int)(__funnelshift_r(lo, hi, sh) & 7u);
                                     hv[u] = __float2half_rn((float)(code - 4) * sf);
                                 }
-                                q[h2] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+                                qv[h2] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
                             }
-                            st_shared_v4(at + sw128_off(r, 4 * b + c), q[0], q[1], q[2], q[3]);
+                            st_shared_v4(at + sw128_off(r, 4 * b + c), qv[0], qv[1], qv[2], qv[3]);
                         }
                     }
                 }
             }
             fence_proxy_async();
-            mbar_arrive(smem_u32(&full_bar[s]));
-            // refill the stage step ks-1 used with step ks + STAGES - 1 once its MMAs are done
-            const int nx = ks + C::STAGES - 1;
-            if (nx < nk) {
-                if (ks >= 1) {
-                    const int ps = (ks - 1) % C::STAGES;
-                    ok = mbar_wait(smem_u32(&empty_bar[ps]), ((ks - 1) / C::STAGES) & 1, abort_flag);
-                }
-                ok = __all_sync(0xffffffffu, ok);
-                __syncwarp();
-                if (ok) issue(nx);
-            }
-            cp_async_commit();
+            mbar_arrive(smem_u32(&a_full[s]));
         }
-        cp_async_wait_all();
-    } else if (warp == 4) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = f16_idesc(kGmM, nround);
-            bool ok = true;
-            for (int ks = 0; ks < nk; ++ks) {
-                const int s = ks % C::STAGES;
-                if (!mbar_wait(smem_u32(&full_bar[s]), (ks / C::STAGES) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tb = smem_u32(tiles_base + (size_t)s * C::TILE_BYTES);
-                const uint32_t bhi_s = tb + C::NA * C::A_BYTES, blo_s = bhi_s + C::B_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < kGmK / 16; ++kk) {
-                    const uint64_t bh = sw128_desc(bhi_s + 32 * kk), bl = sw128_desc(blo_s + 32 * kk);
-#pragma unroll
-                    for (int m = 0; m < C::NA; ++m) {
-                        const uint64_t ad = sw128_desc(tb + m * C::A_BYTES + 32 * kk);
-                        const uint32_t acc_col = tmem + (uint32_t)(m * kGmN);
-                        mma_f16(acc_col, ad, bh, idesc, (ks | kk) != 0);
-                        mma_f16(acc_col, ad, bl, idesc, 1u);
-                    }
-                }
-                mma_commit(smem_u32(&empty_bar[s]));
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int et = tid - 192;                 // 0..127: table entry this thread loads
+        const int row = 32 * (warp & 3) + lane;   // accumulator lane = weight row
+        const uint32_t tl_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        bool dead = false;  // after an abort the loop still meets every named barrier
+        for (int j = 0; j < nq; ++j) {
+            Tile tl;
+            int m0;
+            item(j, tl, m0);
+            const int buf = j & 1, p0 = tl.p0, nval = tl.n, nround = (nval + 15) & ~15;
+            {
+                const int p = p0 + min(et, nval - 1);
+                const int t = a.perm_tok[p];
+                s_tok[buf * kGmN + et] = t;
+                s_exp[buf * kGmN + et] = a.brow_exp[p];
+                s_wt[buf * kGmN + et] = (!GATEUP && a.w) ? a.w[(size_t)t * a.k + a.perm_slot[p]] : 0.f;
             }
-            (void)ok;
-            mma_commit(smem_u32(acc_bar));  // completes when every MMA issued above is done
-        }
-        __syncwarp();
-    }
-
-    if (warp >= 4) {
-        // ------------------------------------------------------ epilogue
-        // the issuer always commits acc_bar, so this wait also drains in-flight MMAs
-        bool ok = mbar_wait(smem_u32(acc_bar), 0, abort_flag, false);
-        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-        tc_fence_after();
-        if (ok) {
-            const int ew = warp - 4;
-            const int row = 32 * ew + lane;  // accumulator lane = A row
-            const uint32_t tl = tmem + ((uint32_t)(32 * ew) << 16);
+            named_sync(1, 128);
+            if (dead) continue;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acc_full[buf]), (j >> 1) & 1, abort_flag))) {
+                dead = true;
+                continue;
+            }
+            tc_fence_after();
+            const int *etab = s_exp + buf * kGmN;
+            const uint32_t acc = tl_lane + (uint32_t)(buf * C::ACC_COLS);
             for (int c0 = 0; c0 < nround; c0 += 16) {
                 float acc0[16];
-                tmem_ld16(tl + (uint32_t)c0, acc0);
+                tmem_ld16(acc + (uint32_t)c0, acc0);
                 if (GATEUP) {
                     float acc1[16];
-                    tmem_ld16(tl + (uint32_t)(kGmN + c0), acc1);
+                    tmem_ld16(acc + (uint32_t)(kGmN + c0), acc1);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const int j = c0 + jj;
-                        if (j >= nval) break;
-                        const float sc = exp2i(s_exp[j]);
-                        const float G = acc0[jj] * sc, U = acc1[jj] * sc;
-                        const float h = __fdiv_rn(G, 1.0f + expf(-G)) * U;
+                        const int jc = c0 + jj;
+                        if (jc >= nval) break;
+                        const float sc = exp2i(etab[jc]);
+                        const float Gv = acc0[jj] * sc, Uv = acc1[jj] * sc;
+                        const float h = __fdiv_rn(Gv, 1.0f + expf(-Gv)) * Uv;
                         const float s = block_scale(warp_absmax(h));
                         const int q = block_code(h, s);
-                        const size_t p = (size_t)(p0 + j);
+                        const size_t p = (size_t)(p0 + jc);
                         a.qh[p * a.I + m0 + row] = (int8_t)q;
                         if (lane == 0) a.sh[p * (a.I / 32) + (m0 + row) / 32] = s;
                     }
                 } else {
+                    const int *ttab = s_tok + buf * kGmN;
+                    const float *wtab = s_wt + buf * kGmN;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const int j = c0 + jj;
-                        if (j >= nval) break;
-                        const float D = acc0[jj] * exp2i(s_exp[j]);
-                        if (a.y) atomicAdd(a.y + (size_t)s_tok[j] * a.H + m0 + row, s_wt[j] * D);
-                        if (a.out_sorted) a.out_sorted[(size_t)(p0 + j) * a.H + m0 + row] = D;
+                        const int jc = c0 + jj;
+                        if (jc >= nval) break;
+                        const float D = acc0[jj] * exp2i(etab[jc]);
+                        if (a.y) atomicAdd(a.y + (size_t)ttab[jc] * a.H + m0 + row, wtab[jc] * D);
+                        if (a.out_sorted) a.out_sorted[(size_t)(p0 + jc) * a.H + m0 + row] = D;
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[buf]));
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
                      : "memory");

@@ -108,10 +108,10 @@ Layout layout(long long T, long long H, long long I, long long E, long long k) {
     L.tiles = take(max_tiles * (long long)sizeof(Tile));
     L.qx = take(T * H);
     L.sx = take(T * (H / 32) * 4);
-    L.ex = take(T * 4);
+    L.ex = take(P * 4);
     L.xsum = take(T * (H / 32) * 4);
-    L.xhi = take(T * H * 2);
-    L.xlo = take(T * H * 2);
+    L.xhi = take(P * H * 2);
+    L.xlo = take(P * H * 2);
     L.qh = take(P * I);
     L.sh = take(P * (I / 32) * 4);
     L.eh = take(P * 4);
@@ -271,9 +271,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 
 // 2-D TMA map over a row-major [rows][cols] array of esize-byte elements with
-// box {box_c, box_r}; no swizzle, zero fill outside the array.
+// box {box_c, box_r}; zero fill outside the array.
 int tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint64_t esize, uint64_t cols, uint64_t rows,
-            uint32_t box_c, uint32_t box_r) {
+            uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (!enc) return fail(MOEQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     cuuint64_t dims[2] = {cols, rows};
@@ -281,7 +281,7 @@ int tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint64_t e
     cuuint32_t box[2] = {box_c, box_r};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOEQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return MOEQ_OK;
 }
@@ -332,17 +332,33 @@ int gemv_dispatch(const GemvArgs &g, int bits, int T, int k, int E, cudaStream_t
 #undef MOEQ_GEMV
 }
 
+int sm_count() {
+    static int v = 0;
+    if (!v) {
+        int dev = 0, val = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&val, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && val > 0)
+            v = val;
+        else
+            v = 148;
+    }
+    return v;
+}
+
+// The persistent grouped GEMM: one CTA per SM (at most one per work item).
 template <bool GATEUP, int BITS>
 int launch_gemm(const GemmArgs &g, long long max_tiles, cudaStream_t s) {
     using C = GemmCfg<GATEUP, BITS>;
+    if ((int)C::SMEM > max_smem_optin()) return fail(MOEQ_ERR_SHAPE, "grouped GEMM needs %zu bytes of shared memory", C::SMEM);
     cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel<GATEUP, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
     const int MT = (GATEUP ? g.I : g.H) / kGmM;
-    const long long blocks = max_tiles * MT;
-    if (blocks == 0) return MOEQ_OK;
+    const long long items = max_tiles * MT;
+    if (items == 0) return MOEQ_OK;
+    const unsigned blocks = (unsigned)std::min<long long>(items, sm_count());
     trace_begin(s);
-    ffn_gemm_kernel<GATEUP, BITS><<<(unsigned)blocks, 256, C::SMEM, s>>>(g);
+    ffn_gemm_kernel<GATEUP, BITS><<<blocks, C::THREADS, C::SMEM, s>>>(g);
     trace_end(s);
     return cuda_check("ffn_gemm_kernel");
 }
@@ -404,8 +420,13 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     float *sh = sh_out ? sh_out : at<float>(ws, L.sh);
     int *eh = at<int>(ws, L.eh);
     __half *hhi = at<__half>(ws, L.hhi), *hlo = at<__half>(ws, L.hlo);
-    quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, xhi, xlo, ex, nullptr, nullptr, nullptr, nullptr, 0);
+    // x quantised per token, then its fp16 hi/lo rows written in sorted pair
+    // order so that every GEMM tile reads contiguous B rows
+    quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0);
     if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
+    const unsigned split_blocks = (unsigned)std::min<long long>((P + 7) / 8, (long long)sm_count() * 16);
+    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, xhi, xlo, ex);
+    if (int rc = cuda_check("split_rows_kernel(x)")) return rc;
     const long long max_tiles = (P + kTileN - 1) / kTileN + E;
     GemmArgs g{};
     g.T = T;
@@ -425,15 +446,25 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     g.bhi = xhi;
     g.blo = xlo;
     g.brow_exp = ex;
+    for (int h = 0; h < 4; ++h)  // hi, lo with 16-row boxes, then with 128-row boxes
+        if (int rc = tmap_2d(&g.bmap[h], (h & 1) ? (const void *)xlo : (const void *)xhi,
+                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)H, (uint64_t)P, kGmK, h < 2 ? 16 : kGmN,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+            return rc;
     g.qh = qh;
     g.sh = sh;
     int rc = bits == 2 ? launch_gemm<true, 2>(g, max_tiles, s) : launch_gemm<true, 3>(g, max_tiles, s);
     if (rc) return rc;
-    quant_rows_kernel<<<(unsigned)P, 256, 0, s>>>(nullptr, I, nullptr, nullptr, hhi, hlo, eh, qh, sh, nullptr, nullptr, 0);
-    if ((rc = cuda_check("quant_rows_kernel(h)"))) return rc;
+    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qh, sh, I, nullptr, (int)P, hhi, hlo, eh);
+    if ((rc = cuda_check("split_rows_kernel(h)"))) return rc;
     g.bhi = hhi;
     g.blo = hlo;
     g.brow_exp = eh;
+    for (int h = 0; h < 4; ++h)
+        if (int rc = tmap_2d(&g.bmap[h], (h & 1) ? (const void *)hlo : (const void *)hhi,
+                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)I, (uint64_t)P, kGmK, h < 2 ? 16 : kGmN,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+            return rc;
     g.y = y;
     g.out_sorted = out_sorted;
     return bits == 2 ? launch_gemm<false, 2>(g, max_tiles, s) : launch_gemm<false, 3>(g, max_tiles, s);

@@ -75,4 +75,48 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict
     }
 }
 
+// fp16 hi/lo operand rows for the tensor-core GEMM: output row r is input row
+// row_map[r] (or r) of q [*, n] int8 with block scales s [*, n/32]; its values
+// q*s*2^-e are split into hi + lo with e = row_exponent(max block scale of the
+// row), written to hi/lo [rows, n] and e_out[r].  One warp per output row, 8
+// values (one 16-byte store of each half) per lane per step.
+__global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restrict__ q, const float *__restrict__ s,
+                                                         int n, const int32_t *__restrict__ row_map, int rows,
+                                                         __half *__restrict__ hi, __half *__restrict__ lo,
+                                                         int *__restrict__ e_out) {
+    const int lane = threadIdx.x & 31;
+    const int nb = n / 32;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
+        const size_t src = row_map ? (size_t)row_map[r] : (size_t)r;
+        const float *sr = s + src * nb;
+        float m = 0.f;
+        for (int b = lane; b < nb; b += 32) m = fmaxf(m, sr[b]);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int e = row_exponent(m);
+        if (lane == 0) e_out[r] = e;
+        const float inv = exp2i(-e);
+        const int8_t *qr = q + src * n;
+        __half *hr = hi + (size_t)r * n;
+        __half *lr = lo + (size_t)r * n;
+        for (int c = lane; c < n / 8; c += 32) {
+            const uint2 qv = *reinterpret_cast<const uint2 *>(qr + 8 * c);
+            const float sc = sr[(8 * c) / 32] * inv;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t word = i < 2 ? qv.x : qv.y;
+                const float v0 = (float)(int8_t)(word >> (16 * (i & 1))) * sc;
+                const float v1 = (float)(int8_t)(word >> (16 * (i & 1) + 8)) * sc;
+                __half h0, l0, h1, l1;
+                split_hi_lo(v0, h0, l0);
+                split_hi_lo(v1, h1, l1);
+                hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            }
+            *reinterpret_cast<uint4 *>(hr + 8 * c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(lr + 8 * c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+    }
+}
+
 }  // namespace moeq
