@@ -23,8 +23,6 @@
 // The kernel is persistent and warp-specialised (see ffn_gemm_kernel).
 #pragma once
 
-#include <cuda.h>
-
 #include "async.cuh"
 #include "permute.cuh"
 
@@ -42,14 +40,15 @@ struct GemmArgs {
     const int *ctrl;  // ctrl[2] = number of tiles
     const int32_t *perm_tok, *perm_slot;
     const float *w;
-    const __half *bhi, *blo;  // B rows by sorted pair position: x of the pair's token (gate/up) or h (down)
-    const int *brow_exp;      // their power-of-two exponents, per sorted pair
+    // B operand image (fp16, see split_rows_kernel): [K/64][hi, lo][bimg_rows][64],
+    // rows = sorted pair positions, chunks pre-swizzled per tile; x of the pair's
+    // token (gate/up) or its h (down)
+    const __half *bimg;
+    long long bimg_rows;
+    const int *brow_exp;  // power-of-two exponents of the B rows, per sorted pair
     int8_t *qh;               // gate/up outputs [T*k, I]
     float *sh;                // [T*k, I/32]
     float *y, *out_sorted;    // down outputs
-    // TMA maps of the B rows (fp16 [P][K], 128-byte swizzle): [0] hi, [1] lo with
-    // 64 x 16-row boxes, [2] hi, [3] lo with 64 x 128-row boxes
-    CUtensorMap bmap[4];
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -94,16 +93,21 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
+// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.  The load
+// and its wait are one asm statement, so no use of the destination registers
+// can be scheduled before the asynchronous load has completed.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
+        "{\n\t"
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
+        "%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "}"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -125,7 +129,10 @@ template <bool GATEUP, int BITS>
 struct GemmCfg {
     static constexpr int NA = GATEUP ? 2 : 1;  // weight matrices per work item (gate + up, or down)
     static constexpr int BPB = 4 * BITS;
-    static constexpr int STAGES = GATEUP ? 3 : 4;                  // operand ring, K = 64 per stage
+    // operand ring, K = 64 per stage.  Two slots: with three or more in flight the
+    // gate/up outputs of some tiles came out wrong intermittently (cause not
+    // found); two slots gave identical results over repeated 4096-token runs.
+    static constexpr int STAGES = 2;
     static constexpr int RSTAGES = (GATEUP && BITS == 3) ? 4 : 6;  // raw-code ring (runs further ahead)
     static constexpr int A_BYTES = kGmM * kGmK * 2;                // fp16 weight tile
     static constexpr int B_BYTES = kGmN * kGmK * 2;                // fp16 activation tile (hi or lo)
@@ -141,17 +148,6 @@ struct GemmCfg {
     static constexpr int THREADS = 320;  // 10 warps, see the kernel
 };
 
-// Four rows (r0..r3) of 64 fp16 starting at column x of a 2-D tensor map with a
-// one-row box, into 4 consecutive 128-byte rows of shared memory (swizzled by
-// the map).  Completes on `bar` (512 bytes).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // Persistent grouped GEMM: one CTA per SM walks the work items q = blockIdx.x,
@@ -159,8 +155,8 @@ __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sy
 // K/64 pipeline stages; stage g of this CTA uses operand slot g % STAGES and
 // raw slot g % RSTAGES, so every role derives the same slot and phase from g.
 //   warp 0     producer: bulk copies of the raw codes/scales (RSTAGES ahead)
-//              and 2-D TMA loads of the tile's B rows (hi, lo; contiguous in
-//              sorted pair order) into the swizzled slots, on mbarriers
+//              and of the tile's B rows (hi, lo: one contiguous, pre-swizzled
+//              run each per K stage) into the operand slots, on mbarriers
 //   warp 1     TMEM owner; lane 0 issues the MMAs (hi and lo per K step)
 //   warps 2-5  unpack: row r of the weight tile, codes -> fp16 level*scale
 //   warps 6-9  epilogue on the other accumulator buffer (TMEM lane quadrant
@@ -224,76 +220,77 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     const uint32_t tmem = *tmem_slot;
 
     // work item j of this CTA -> (tile, first weight row)
-    auto item = [&](int j, Tile &tl, int &m0) {
-        const int q = (int)blockIdx.x + j * (int)gridDim.x;
-        tl = a.tiles[q / MT];
-        m0 = (q % MT) * kGmM;
-    };
+    auto item_tile = [&](int j) { return a.tiles[((int)blockIdx.x + j * (int)gridDim.x) / MT]; };
+    auto item_m0 = [&](int j) { return (((int)blockIdx.x + j * (int)gridDim.x) % MT) * kGmM; };
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane < 4) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.bmap[lane])) : "memory");
         const uint64_t pol = l2_evict_first();
-        int graw = 0, raw_j = -1, raw_m0 = 0;
-        Tile raw_tl{};
-        int b_j = -1;
-        Tile b_tl{};
-        int gb = 0;                 // B stages issued
+        // raw cursor: runs up to R stages ahead of the operand cursor
+        int rj = 0, rks = 0, rs = 0, graw = 0;
+        uint32_t rph = 0;
+        Tile rtl = nq > 0 ? item_tile(0) : Tile{};
+        int rm0 = nq > 0 ? item_m0(0) : 0;
+        int s = 0, gb = 0;
+        uint32_t ph = 0;
         bool ok = true;
-        for (int g = 0; g < G && ok; ++g) {
-            // raw codes/scales, up to R stages ahead of the operands
-            for (; graw < G && graw < g + R; ++graw) {
-                const int j = graw / nk, ks = graw - j * nk;
-                if (j != raw_j) {
-                    item(j, raw_tl, raw_m0);
-                    raw_j = j;
+        for (int j = 0; j < nq && ok; ++j) {
+            const Tile tl = item_tile(j);
+            const int nround = (tl.n + 15) & ~15;
+            for (int ks = 0; ks < nk; ++ks) {
+                const int g = j * nk + ks;
+                for (; graw < G && graw < g + R; ++graw) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&raw_empty[rs]), rph ^ 1, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t rbar = smem_u32(&raw_full[rs]);
+                    if (lane == 0) mbar_arrive_expect_tx(rbar, (uint32_t)C::RAW_BYTES);
+                    __syncwarp();
+                    if (lane < 4 * NA) {  // lanes [0, 2NA): codes of (matrix, block); [2NA, 4NA): scales
+                        const int mb = lane % (2 * NA), m = mb >> 1, kb = 2 * rks + (mb & 1);
+                        const int mat = GATEUP ? m : 2;
+                        const size_t blk = ((size_t)rtl.e * KB + kb) * NR + rm0;
+                        unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
+                        if (lane < 2 * NA)
+                            bulk_g2s(smem_u32(rw + mb * kGmM * BPB), a.codes[mat] + blk * BPB, kGmM * BPB, rbar, pol);
+                        else
+                            bulk_g2s(smem_u32(rw + C::RAW_CODES + mb * kGmM * 2), a.scales[mat] + blk, kGmM * 2, rbar,
+                                     pol);
+                    }
+                    if (++rs == R) {
+                        rs = 0;
+                        rph ^= 1;
+                    }
+                    if (++rks == nk) {
+                        rks = 0;
+                        if (++rj < nq) {
+                            rtl = item_tile(rj);
+                            rm0 = item_m0(rj);
+                        }
+                    }
                 }
-                const int rs = graw % R;
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&raw_empty[rs]), ((graw / R) & 1) ^ 1, abort_flag))) {
+                if (!ok) break;
+                // B rows of this stage: hi/lo of sorted pairs p0 .. p0 + nround, K columns
+                // [64 ks, 64 ks + 64), one contiguous run of 128-byte rows per half
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag))) {
                     ok = false;
                     break;
                 }
-                const uint32_t rbar = smem_u32(&raw_full[rs]);
-                if (lane == 0) mbar_arrive_expect_tx(rbar, (uint32_t)C::RAW_BYTES);
+                const uint32_t bbar = smem_u32(&b_full[s]);
+                const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + NA * C::A_BYTES), blo = bhi + C::B_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(2 * nround * kGmK * 2));
                 __syncwarp();
-                if (lane < 4 * NA) {  // lanes [0, 2NA): codes of (matrix, block); [2NA, 4NA): scales
-                    const int mb = lane % (2 * NA), m = mb >> 1, kb = 2 * ks + (mb & 1);
-                    const int mat = GATEUP ? m : 2;
-                    const size_t blk = ((size_t)raw_tl.e * KB + kb) * NR + raw_m0;
-                    unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
-                    if (lane < 2 * NA)
-                        bulk_g2s(smem_u32(rw + mb * kGmM * BPB), a.codes[mat] + blk * BPB, kGmM * BPB, rbar, pol);
-                    else
-                        bulk_g2s(smem_u32(rw + C::RAW_CODES + mb * kGmM * 2), a.scales[mat] + blk, kGmM * 2, rbar, pol);
+                if (lane < 2)
+                    bulk_g2s(lane ? blo : bhi,
+                             a.bimg + ((size_t)(2 * ks + lane) * (size_t)a.bimg_rows + (size_t)tl.p0) * kGmK,
+                             (uint32_t)(nround * kGmK * 2), bbar, 0);
+                gb = g + 1;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
                 }
             }
-            if (!ok) break;
-            // B rows of stage g: activations hi/lo of sorted pairs p0 .. p0 + nround,
-            // K columns [64 ks, 64 ks + 64): one 128-row box per half for a full
-            // tile, else one 16-row box per 16 rows (lane i: rows 16 i ..)
-            const int j = g / nk, ks = g - j * nk;
-            if (j != b_j) {
-                int m0u;
-                item(j, b_tl, m0u);
-                b_j = j;
-            }
-            const int s = g % S;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&slot_empty[s]), ((g / S) & 1) ^ 1, abort_flag))) {
-                ok = false;
-                break;
-            }
-            const int nround = (b_tl.n + 15) & ~15;
-            const uint32_t bbar = smem_u32(&b_full[s]);
-            const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + NA * C::A_BYTES), blo = bhi + C::B_BYTES;
-            if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(2 * nround * kGmK * 2));
-            __syncwarp();
-            if (nround == kGmN) {
-                if (lane < 2) tma_load_2d(lane ? blo : bhi, &a.bmap[2 + lane], ks * kGmK, b_tl.p0, bbar, 0);
-            } else if (16 * lane < nround) {
-                tma_load_2d(bhi + 2048 * lane, &a.bmap[0], ks * kGmK, b_tl.p0 + 16 * lane, bbar, 0);
-                tma_load_2d(blo + 2048 * lane, &a.bmap[1], ks * kGmK, b_tl.p0 + 16 * lane, bbar, 0);
-            }
-            gb = g + 1;
         }
         if (!ok && lane == 0) {  // drain the copies still in flight
             for (int g2 = max(0, graw - R); g2 < graw; ++g2)
@@ -304,41 +301,45 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
-            int cur_j = -1;
-            uint32_t idesc = 0;
-            for (int g = 0; g < G; ++g) {
-                const int j = g / nk, ks = g - j * nk, buf = j & 1;
-                if (j != cur_j) {
-                    Tile tl;
-                    int m0;
-                    item(j, tl, m0);
-                    idesc = f16_idesc(kGmM, (tl.n + 15) & ~15);
-                    cur_j = j;
-                }
-                if (ks == 0) {
-                    if (!mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag)) break;
-                    tc_fence_after();
-                }
-                const int s = g % S;
-                const uint32_t ph = (g / S) & 1;
-                if (!mbar_wait(smem_u32(&a_full[s]), ph, abort_flag)) break;
-                if (!mbar_wait(smem_u32(&b_full[s]), ph, abort_flag)) break;
+            // descriptors: slot s, matrix m, K step kk = base + ((s*SLOT + m*A) >> 4) + 2 kk
+            const uint64_t d0 = sw128_desc(smem_u32(slots));
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            Tile next = nq > 0 ? item_tile(0) : Tile{};
+            for (int j = 0; j < nq && ok; ++j) {
+                const Tile tl = next;
+                if (j + 1 < nq) next = item_tile(j + 1);  // consumed one item later
+                const uint32_t idesc = f16_idesc(kGmM, (tl.n + 15) & ~15);
+                const int buf = j & 1;
+                if (!mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t sb = smem_u32(slots + (size_t)s * C::SLOT_BYTES);
-                const uint32_t bhi = sb + NA * C::A_BYTES, blo = bhi + C::B_BYTES;
+                const uint32_t acc0 = tmem + (uint32_t)(buf * C::ACC_COLS);
+                for (int ks = 0; ks < nk; ++ks) {
+                    if (!mbar_wait(smem_u32(&a_full[s]), ph, abort_flag) || !mbar_wait(smem_u32(&b_full[s]), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ds = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
+                    const uint64_t dbh = ds + (uint64_t)((NA * C::A_BYTES) >> 4), dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kGmK / 16; ++kk) {
-                    const uint64_t bh = sw128_desc(bhi + 32 * kk), bl = sw128_desc(blo + 32 * kk);
+                    for (int kk = 0; kk < kGmK / 16; ++kk) {
 #pragma unroll
-                    for (int m = 0; m < NA; ++m) {
-                        const uint64_t ad = sw128_desc(sb + m * C::A_BYTES + 32 * kk);
-                        const uint32_t acc = tmem + (uint32_t)(buf * C::ACC_COLS + m * kGmN);
-                        mma_f16(acc, ad, bh, idesc, (ks | kk) != 0);
-                        mma_f16(acc, ad, bl, idesc, 1u);
+                        for (int m = 0; m < NA; ++m) {
+                            const uint64_t ad = ds + (uint64_t)((m * C::A_BYTES) >> 4) + 2 * kk;
+                            const uint32_t acc = acc0 + (uint32_t)(m * kGmN);
+                            mma_f16(acc, ad, dbh + 2 * kk, idesc, (ks | kk) != 0);
+                            mma_f16(acc, ad, dbl + 2 * kk, idesc, 1u);
+                        }
+                    }
+                    mma_commit(smem_u32(&slot_empty[s]));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1;
                     }
                 }
-                mma_commit(smem_u32(&slot_empty[s]));
-                if (ks == nk - 1) mma_commit(smem_u32(&acc_full[buf]));
+                if (ok) mma_commit(smem_u32(&acc_full[buf]));
             }
             // every MMA issued above is complete once this commit lands
             mma_commit(smem_u32(drain));
@@ -348,9 +349,11 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp < 6) {
         // ----------------------------------------------------------- unpack
         const int r = tid - 64;  // weight row of the tile
-        for (int g = 0; g < G; ++g) {
-            const int rs = g % R;
-            if (!mbar_wait(smem_u32(&raw_full[rs]), (g / R) & 1, abort_flag)) break;
+        int rs = 0, s = 0;
+        uint32_t rph = 0, ph = 0;
+        bool ok = true;
+        for (int g = 0; g < G && ok; ++g) {
+            if (!mbar_wait(smem_u32(&raw_full[rs]), rph, abort_flag)) break;
             const unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
             uint32_t cw[NA][2][BITS];
             uint16_t sbits[NA][2];
@@ -364,8 +367,11 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     sbits[m][b] = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + r) * 2);
                 }
             mbar_arrive(smem_u32(&raw_empty[rs]));
-            const int s = g % S;
-            if (!mbar_wait(smem_u32(&slot_empty[s]), ((g / S) & 1) ^ 1, abort_flag)) break;
+            if (++rs == R) {
+                rs = 0;
+                rph ^= 1;
+            }
+            if (!mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag)) break;
             unsigned char *sb = slots + (size_t)s * C::SLOT_BYTES;
 #pragma unroll
             for (int m = 0; m < NA; ++m) {
@@ -414,6 +420,10 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             }
             fence_proxy_async();
             mbar_arrive(smem_u32(&a_full[s]));
+            if (++s == S) {
+                s = 0;
+                ph ^= 1;
+            }
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -422,9 +432,8 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
         const uint32_t tl_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         bool dead = false;  // after an abort the loop still meets every named barrier
         for (int j = 0; j < nq; ++j) {
-            Tile tl;
-            int m0;
-            item(j, tl, m0);
+            const Tile tl = item_tile(j);
+            const int m0 = item_m0(j);
             const int buf = j & 1, p0 = tl.p0, nval = tl.n, nround = (nval + 15) & ~15;
             {
                 const int p = p0 + min(et, nval - 1);

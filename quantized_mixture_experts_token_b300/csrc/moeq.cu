@@ -79,8 +79,9 @@ constexpr int kFusedRouteMaxT = kFusedMaxT;  // (the router kernel's tail handle
 constexpr int kInCtaRouteMaxT = 2;
 
 struct Layout {
-    size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, units, tiles, qx, sx,
-        ex, xsum, xhi, xlo, qh, sh, eh, hhi, hlo, total;
+    size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, chunk_count, chunk_base, units,
+        tiles, qx, sx,
+        ex, xsum, ximg, qh, sh, eh, himg, total;
 };
 
 Layout layout(long long T, long long H, long long I, long long E, long long k) {
@@ -104,19 +105,20 @@ Layout layout(long long T, long long H, long long I, long long E, long long k) {
     L.inv = take(P * 4);
     L.masks = take(E * W * 4);
     L.prefix = take(E * W * 4);
+    const long long NC = (W + kPermChunkWords - 1) / kPermChunkWords;
+    L.chunk_count = take(NC * E * 4);
+    L.chunk_base = take(NC * E * 4);
     L.units = take(E * (long long)sizeof(UnitRec));
     L.tiles = take(max_tiles * (long long)sizeof(Tile));
     L.qx = take(T * H);
     L.sx = take(T * (H / 32) * 4);
     L.ex = take(P * 4);
     L.xsum = take(T * (H / 32) * 4);
-    L.xhi = take(P * H * 2);
-    L.xlo = take(P * H * 2);
+    L.ximg = take(2 * (P + kTileN) * H * 2);  // hi + lo operand image, 128 rows of slack
     L.qh = take(P * I);
     L.sh = take(P * (I / 32) * 4);
     L.eh = take(P * 4);
-    L.hhi = take(P * I * 2);
-    L.hlo = take(P * I * 2);
+    L.himg = take(2 * (P + kTileN) * I * 2);
     L.total = off;
     return L;
 }
@@ -363,6 +365,21 @@ int launch_gemm(const GemmArgs &g, long long max_tiles, cudaStream_t s) {
     return cuda_check("ffn_gemm_kernel");
 }
 
+// The token-to-expert permutation on the whole GPU (three small kernels).
+int permute_multi(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets, int32_t *perm_tok,
+                  int32_t *perm_slot, int32_t *inv, void *ws, const Layout &L, cudaStream_t s) {
+    const int W = (T + 31) / 32, NC = (W + kPermChunkWords - 1) / kPermChunkWords;
+    unsigned *masks = at<unsigned>(ws, L.masks);
+    int *wprefix = at<int>(ws, L.prefix), *ccount = at<int>(ws, L.chunk_count), *cbase = at<int>(ws, L.chunk_base);
+    permute_count_kernel<<<NC, 256, 0, s>>>(idx, T, k, E, masks, wprefix, ccount);
+    permute_scan_kernel<<<1, 1024, 0, s>>>(NC, E, ccount, cbase, counts, offsets);
+    const long long P = (long long)T * k;
+    const unsigned blocks = (unsigned)std::min<long long>((P + 255) / 256, (long long)sm_count() * 8);
+    permute_scatter_kernel<<<blocks, 256, 0, s>>>(idx, T, k, E, masks, wprefix, cbase, offsets, perm_tok, perm_slot,
+                                                  inv);
+    return cuda_check("permute kernels");
+}
+
 // Experts over an existing permutation.
 int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t *offsets, const int32_t *perm_tok,
             const int32_t *perm_slot, const float *w, float *out_sorted, float *y, int residual, int mode,
@@ -415,17 +432,19 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     int8_t *qx = at<int8_t>(ws, L.qx);
     float *sx = at<float>(ws, L.sx);
     int *ex = at<int>(ws, L.ex);
-    __half *xhi = at<__half>(ws, L.xhi), *xlo = at<__half>(ws, L.xlo);
+    __half *ximg = at<__half>(ws, L.ximg);
     int8_t *qh = qh_out ? qh_out : at<int8_t>(ws, L.qh);
     float *sh = sh_out ? sh_out : at<float>(ws, L.sh);
     int *eh = at<int>(ws, L.eh);
-    __half *hhi = at<__half>(ws, L.hhi), *hlo = at<__half>(ws, L.hlo);
+    __half *himg = at<__half>(ws, L.himg);
+    const long long img_rows = P + kTileN;  // a tile's rows may run up to 127 past P
     // x quantised per token, then its fp16 hi/lo rows written in sorted pair
-    // order so that every GEMM tile reads contiguous B rows
+    // order (pre-swizzled per tile) so that every GEMM tile reads one
+    // contiguous run of B rows per K stage
     quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0);
     if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
     const unsigned split_blocks = (unsigned)std::min<long long>((P + 7) / 8, (long long)sm_count() * 16);
-    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, xhi, xlo, ex);
+    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, offsets, E, ximg, img_rows, ex);
     if (int rc = cuda_check("split_rows_kernel(x)")) return rc;
     const long long max_tiles = (P + kTileN - 1) / kTileN + E;
     GemmArgs g{};
@@ -443,28 +462,17 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     g.perm_tok = perm_tok;
     g.perm_slot = perm_slot;
     g.w = w;
-    g.bhi = xhi;
-    g.blo = xlo;
+    g.bimg = ximg;
+    g.bimg_rows = img_rows;
     g.brow_exp = ex;
-    for (int h = 0; h < 4; ++h)  // hi, lo with 16-row boxes, then with 128-row boxes
-        if (int rc = tmap_2d(&g.bmap[h], (h & 1) ? (const void *)xlo : (const void *)xhi,
-                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)H, (uint64_t)P, kGmK, h < 2 ? 16 : kGmN,
-                             CU_TENSOR_MAP_SWIZZLE_128B))
-            return rc;
     g.qh = qh;
     g.sh = sh;
     int rc = bits == 2 ? launch_gemm<true, 2>(g, max_tiles, s) : launch_gemm<true, 3>(g, max_tiles, s);
     if (rc) return rc;
-    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qh, sh, I, nullptr, (int)P, hhi, hlo, eh);
+    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qh, sh, I, nullptr, (int)P, offsets, E, himg, img_rows, eh);
     if ((rc = cuda_check("split_rows_kernel(h)"))) return rc;
-    g.bhi = hhi;
-    g.blo = hlo;
+    g.bimg = himg;
     g.brow_exp = eh;
-    for (int h = 0; h < 4; ++h)
-        if (int rc = tmap_2d(&g.bmap[h], (h & 1) ? (const void *)hlo : (const void *)hhi,
-                             CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)I, (uint64_t)P, kGmK, h < 2 ? 16 : kGmN,
-                             CU_TENSOR_MAP_SWIZZLE_128B))
-            return rc;
     g.y = y;
     g.out_sorted = out_sorted;
     return bits == 2 ? launch_gemm<false, 2>(g, max_tiles, s) : launch_gemm<false, 3>(g, max_tiles, s);
@@ -558,10 +566,10 @@ int moe_permute(const int32_t *idx, int T, int k, int E, int32_t *counts_out, in
     REQ_PTR(inv_out);
     const Layout L = layout(T, 128, 128, E, k);
     if (!ws || !aligned(ws, 256)) return fail(MOEQ_ERR_ALIGN, "ws missing or not 256-byte aligned");
-    if (ws_bytes < L.prefix + (size_t)E * ((T + 31) / 32) * 4) return fail(MOEQ_ERR_WORKSPACE, "workspace too small");
-    permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, at<unsigned>(ws, L.masks), at<int>(ws, L.prefix), counts_out,
-                                      offsets_out, perm_tok_out, perm_slot_out, inv_out);
-    if (int rc = cuda_check("permute_kernel")) return rc;
+    if (ws_bytes < L.chunk_base + (size_t)E * (((T + 31) / 32 + kPermChunkWords - 1) / kPermChunkWords) * 4)
+        return fail(MOEQ_ERR_WORKSPACE, "workspace too small");
+    if (int rc = permute_multi(idx, T, k, E, counts_out, offsets_out, perm_tok_out, perm_slot_out, inv_out, ws, L, s))
+        return rc;
     return ok();
 }
 
@@ -731,9 +739,7 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
     }
     if (int rc = route_unfused(x, T, H, Wr, bias, E, k, idx, w, at<float>(ws, L.logits), s)) return rc;
     if (int rc = cuda_check("route")) return rc;
-    permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, at<unsigned>(ws, L.masks), at<int>(ws, L.prefix), counts, offsets,
-                                      perm_tok, perm_slot, inv);
-    if (int rc = cuda_check("permute_kernel")) return rc;
+    if (int rc = permute_multi(idx, T, k, E, counts, offsets, perm_tok, perm_slot, inv, ws, L, s)) return rc;
     if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, nullptr, y_out, residual, mode, nullptr,
                          nullptr, ws, L, s))
         return rc;

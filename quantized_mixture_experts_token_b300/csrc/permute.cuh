@@ -62,6 +62,89 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict
     }
 }
 
+// ---------------------------------------------------------------- multi-CTA
+// The same stable counting sort spread over the GPU, for large T.  Tokens are
+// split into chunks of kPermChunkWords 32-token words.
+//   permute_count_kernel   one CTA per chunk: the chunk's token bitmaps of
+//                          every expert (shared-memory atomics), their
+//                          prefix popcounts inside the chunk, and the chunk's
+//                          count per expert;
+//   permute_scan_kernel    one CTA: per-expert chunk bases (scan over chunks),
+//                          counts, offsets (scan over experts);
+//   permute_scatter_kernel one thread per pair: rank = chunk base + prefix of
+//                          the words before it + popcount of the bits below.
+constexpr int kPermChunkWords = 8;  // 256 tokens per chunk
+
+__global__ void __launch_bounds__(256) permute_count_kernel(const int32_t *__restrict__ idx, int T, int k, int E,
+                                                            unsigned *masks /* [E][W] */, int *wprefix /* [E][W] */,
+                                                            int *chunk_count /* [NC][E] */) {
+    __shared__ unsigned s_mask[kMaxE * kPermChunkWords];
+    const int W = (T + 31) / 32, c = blockIdx.x;
+    const int w0 = c * kPermChunkWords, nw = min(kPermChunkWords, W - w0);
+    for (int i = threadIdx.x; i < E * kPermChunkWords; i += blockDim.x) s_mask[i] = 0u;
+    __syncthreads();
+    const int t0 = w0 * 32, t1 = min(T, (w0 + nw) * 32);
+    for (int p = t0 * k + threadIdx.x; p < t1 * k; p += blockDim.x) {
+        const int e = idx[p], t = p / k;
+        if (e < 0 || e >= E) {
+            set_status(MOEQ_STATUS_BAD_INDEX);
+            continue;
+        }
+        atomicOr(&s_mask[e * kPermChunkWords + (t >> 5) - w0], 1u << (t & 31));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int i = 0; i < nw; ++i) {
+            const unsigned m = s_mask[e * kPermChunkWords + i];
+            masks[(size_t)e * W + w0 + i] = m;
+            wprefix[(size_t)e * W + w0 + i] = run;
+            run += __popc(m);
+        }
+        chunk_count[(size_t)c * E + e] = run;
+    }
+}
+
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int NC, int E, const int *__restrict__ chunk_count,
+                                                            int *chunk_base /* [NC][E] */, int32_t *counts,
+                                                            int32_t *offsets) {
+    __shared__ int s_off[kMaxE];
+    __shared__ int s_scan[33];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < NC; ++c) {
+            chunk_base[(size_t)c * E + e] = run;
+            run += chunk_count[(size_t)c * E + e];
+        }
+        counts[e] = run;
+        s_off[e] = run;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan(s_off, E, s_scan);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = s_off[e];
+    if (threadIdx.x == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(256) permute_scatter_kernel(const int32_t *__restrict__ idx, int T, int k, int E,
+                                                              const unsigned *__restrict__ masks,
+                                                              const int *__restrict__ wprefix,
+                                                              const int *__restrict__ chunk_base,
+                                                              const int32_t *__restrict__ offsets, int32_t *perm_tok,
+                                                              int32_t *perm_slot, int32_t *inv) {
+    const int W = (T + 31) / 32, P = T * k;
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
+        const int e = idx[p], t = p / k, j = p - t * k;
+        if (e < 0 || e >= E) continue;
+        const int w = t >> 5;
+        const size_t wi = (size_t)e * W + w;
+        const int pos = offsets[e] + chunk_base[(size_t)(w / kPermChunkWords) * E + e] + wprefix[wi] +
+                        __popc(masks[wi] & ((1u << (t & 31)) - 1u));
+        perm_tok[pos] = t;
+        perm_slot[pos] = j;
+        inv[p] = pos;
+    }
+}
+
 // Work plan from offsets: the number of experts with at least one pair and
 // their UnitRec records (for the decode expert kernel; units may be NULL), and
 // the list of (expert, first sorted position, rows) tiles of up to kTileN

@@ -75,18 +75,38 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict
     }
 }
 
-// fp16 hi/lo operand rows for the tensor-core GEMM: output row r is input row
-// row_map[r] (or r) of q [*, n] int8 with block scales s [*, n/32]; its values
-// q*s*2^-e are split into hi + lo with e = row_exponent(max block scale of the
-// row), written to hi/lo [rows, n] and e_out[r].  One warp per output row, 8
-// values (one 16-byte store of each half) per lane per step.
+// fp16 hi/lo operand image for the tensor-core GEMM.  Output row r (a sorted
+// pair position) is input row row_map[r] (or r) of q [*, n] int8 with block
+// scales s [*, n/32]; its values q*s*2^-e are split into hi + lo with
+// e = row_exponent(max block scale of the row), e_out[r] = e.
+//
+// The image is laid out so that a GEMM tile's operand for one K stage is one
+// contiguous run of rows that lands in shared memory already in the 128-byte
+// swizzled K-major form the MMA descriptors expect:
+//   img[st][half][row][64]  (st = K stage of 64 values, half 0 = hi, 1 = lo,
+//                            rows = img_rows >= rows + 128 per (st, half))
+// and the 16-byte chunk c of a 128-byte stage row is stored at chunk
+// c ^ ((r - t0) & 7), t0 = the first row of r's tile.  Tiles start at every
+// 128th position of each expert's segment [offsets[e], offsets[e+1]), so the
+// phase is (r - offsets[e]) & 7.  One warp per output row, one 16-byte chunk
+// of each half per lane per step.
 __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restrict__ q, const float *__restrict__ s,
                                                          int n, const int32_t *__restrict__ row_map, int rows,
-                                                         __half *__restrict__ hi, __half *__restrict__ lo,
+                                                         const int32_t *__restrict__ offsets, int E,
+                                                         __half *__restrict__ img, long long img_rows,
                                                          int *__restrict__ e_out) {
     const int lane = threadIdx.x & 31;
     const int nb = n / 32;
+    const size_t half_stride = (size_t)img_rows * 64;  // elements of one (stage, half) plane
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
+        // expert segment of r: the last e with offsets[e] <= r
+        int lo_e = 0, hi_e = E;  // invariant offsets[lo_e] <= r < offsets[hi_e]
+        while (hi_e - lo_e > 1) {
+            const int mid = (lo_e + hi_e) >> 1;
+            if (offsets[mid] <= r) lo_e = mid;
+            else hi_e = mid;
+        }
+        const uint32_t phase = (uint32_t)(r - offsets[lo_e]) & 7u;
         const size_t src = row_map ? (size_t)row_map[r] : (size_t)r;
         const float *sr = s + src * nb;
         float m = 0.f;
@@ -96,8 +116,6 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restric
         if (lane == 0) e_out[r] = e;
         const float inv = exp2i(-e);
         const int8_t *qr = q + src * n;
-        __half *hr = hi + (size_t)r * n;
-        __half *lr = lo + (size_t)r * n;
         for (int c = lane; c < n / 8; c += 32) {
             const uint2 qv = *reinterpret_cast<const uint2 *>(qr + 8 * c);
             const float sc = sr[(8 * c) / 32] * inv;
@@ -113,8 +131,10 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restric
                 hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
                 lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
             }
-            *reinterpret_cast<uint4 *>(hr + 8 * c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(lr + 8 * c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            const size_t st = (size_t)(c >> 3);
+            const size_t off = (size_t)r * 64 + ((((uint32_t)c & 7u) ^ phase) << 3);
+            *reinterpret_cast<uint4 *>(img + (2 * st) * half_stride + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(img + (2 * st + 1) * half_stride + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
     }
 }
