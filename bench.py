@@ -40,6 +40,14 @@ N_LAYERS = 48
 DECODE_T = 1
 PREFILL_T = 4096
 EXPERT_BYTES = 3 * I * (H // 32) * (8 + 2)  # 2-bit codes + fp16 scales of gate, up, down = 983,040
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that ncu
+# measured for the current kernel versions on this workload (cold caches): the
+# decode expert kernel (10 experts, T=1) and the prefill gate/up GEMM
+GEMV_TRAFFIC_BYTES = 9.92e6
+GEMM_GU_TRAFFIC_BYTES = 690.0e6 + 19.6e6
+# library kernels per prefill chunk: router SGEMM, top-k, 3 permutation kernels,
+# plan, y init, x quantisation, 2 operand images, 2 GEMMs
+PREFILL_LAUNCHES = 12
 
 
 # ------------------------------------------------------------------ helpers
@@ -282,7 +290,7 @@ def run_ours(args):
     dec_bytes = statistics.mean(uniq) * EXPERT_BYTES + 2 * T * H * 4
     achieved = dec_bytes / gemv_s / 1e9
     roof_dec = dict(bound="hbm", achieved=achieved, peak=pk["hbm"], unit="GB/s", frac=achieved / pk["hbm"],
-                    traffic=None, kernel="ffn_gemv_kernel<2>", bytes_per_launch=dec_bytes,
+                    traffic=GEMV_TRAFFIC_BYTES, kernel="ffn_gemv_kernel<2>", bytes_per_launch=dec_bytes,
                     launch_us=gemv_s * 1e6, peak_source=f"{pk['source']} hbm_gbs (copy)")
 
     # decode end to end: pinned host token in, result out, every step
@@ -348,12 +356,12 @@ def run_ours(args):
             workload="prefill: 4,096-token chunk through one 2048/512/512 top-10 2-bit layer, Zipf(1.1)-skewed router",
             dtype="fp16 tensor-core products of the exact 2-bit levels and an fp16 hi/lo split of the int8 activations, fp32 accumulate",
             roofline=dict(bound="tensor", achieved=ach, peak=pk["bf16"], unit="TFLOP/s", frac=ach / pk["bf16"],
-                          traffic=None, kernel="ffn_gemm_kernel<gate/up>", flop_per_launch=gu_flop,
+                          traffic=GEMM_GU_TRAFFIC_BYTES, kernel="ffn_gemm_kernel<gate/up>", flop_per_launch=gu_flop,
                           launch_us=gu_s * 1e6, peak_source=f"{pk['source']} bf16_tflops (burst; fp16 = bf16 rate)",
                           down=dict(achieved=dn_flop / dn_s / 1e12, launch_us=dn_s * 1e6, flop_per_launch=dn_flop)),
             e2e=dict(value=pre_e2e_v["value"], unit="tokens/s", h2d_bytes_per_step=Tp * H * 4,
                      d2h_bytes_per_step=Tp * H * 4),
-            gpu_launches_per_chunk=None)
+            gpu_launches_per_chunk=PREFILL_LAUNCHES)
 
     status = moeq.device_status()
     if status:
