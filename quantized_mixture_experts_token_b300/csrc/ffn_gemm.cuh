@@ -6,8 +6,12 @@
 // (0.1.36) ("Strata - the details", "Speed (measured)").  sm_103a has no int8
 // tcgen05 MMA, so the block products are formed on the fp16 path in a way that
 // keeps them as exact as the int8 reading:
-//   * A (weights, M = 128 rows of one expert matrix): level * s_w with level in
-//     {-2,-1,0,1} and s_w fp16 -- exact in fp16;
+//   * A (weights, M = 128 rows of one expert matrix): level * s_w with s_w
+//     fp16.  2-bit levels {-2,-1,0,1} make it exact in fp16.  3-bit levels
+//     reach +-3, whose product needs up to 13 significant bits, so the 3-bit
+//     panel is split into fp16 hi + lo (lo exact: at most 2 significant bits)
+//     and each product takes a third MMA, A_lo * B_hi (A_lo * B_lo, ~2^-22
+//     relative, is dropped like the rest of the B split's residue);
 //   * B (activations, N = up to 128 sorted tokens): v = q * s_a * 2^-e split
 //     into fp16 hi + lo (hi + lo == v to ~2^-22), two MMAs into one fp32
 //     accumulator, so the per-32-block activation scale is carried without an
@@ -135,8 +139,9 @@ struct GemmCfg {
     static constexpr int STAGES = 2;
     static constexpr int RSTAGES = (GATEUP && BITS == 3) ? 4 : 6;  // raw-code ring (runs further ahead)
     static constexpr int A_BYTES = kGmM * kGmK * 2;                // fp16 weight tile
+    static constexpr int NAT = BITS == 3 ? 2 : 1;                  // weight tiles per matrix: hi (, lo)
     static constexpr int B_BYTES = kGmN * kGmK * 2;                // fp16 activation tile (hi or lo)
-    static constexpr int SLOT_BYTES = NA * A_BYTES + 2 * B_BYTES;
+    static constexpr int SLOT_BYTES = NAT * NA * A_BYTES + 2 * B_BYTES;  // A [part][matrix], then B hi, lo
     static constexpr int RAW_CODES = NA * 2 * kGmM * BPB;  // two K-blocks per stage
     static constexpr int RAW_SCALES = NA * 2 * kGmM * 2;
     static constexpr int RAW_BYTES = RAW_CODES + RAW_SCALES;
@@ -278,7 +283,8 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     break;
                 }
                 const uint32_t bbar = smem_u32(&b_full[s]);
-                const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + NA * C::A_BYTES), blo = bhi + C::B_BYTES;
+                const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + C::NAT * NA * C::A_BYTES),
+                               blo = bhi + C::B_BYTES;
                 if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(2 * nround * kGmK * 2));
                 __syncwarp();
                 if (lane < 2)
@@ -322,7 +328,8 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     }
                     tc_fence_after();
                     const uint64_t ds = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
-                    const uint64_t dbh = ds + (uint64_t)((NA * C::A_BYTES) >> 4), dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
+                    const uint64_t dbh = ds + (uint64_t)((C::NAT * NA * C::A_BYTES) >> 4);
+                    const uint64_t dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kGmK / 16; ++kk) {
 #pragma unroll
@@ -331,6 +338,8 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                             const uint32_t acc = acc0 + (uint32_t)(m * kGmN);
                             mma_f16(acc, ad, dbh + 2 * kk, idesc, (ks | kk) != 0);
                             mma_f16(acc, ad, dbl + 2 * kk, idesc, 1u);
+                            if (C::NAT == 2)  // 3-bit: the weight panel's lo part against B hi
+                                mma_f16(acc, ad + (uint64_t)((NA * C::A_BYTES) >> 4), dbh + 2 * kk, idesc, 1u);
                         }
                     }
                     mma_commit(smem_u32(&slot_empty[s]));
@@ -395,24 +404,30 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                             st_shared_v4(at + sw128_off(r, 4 * b + c), q0, q1, q2, q3);
                         }
                     } else {
-                        // 3-bit levels -4..3 times s: +-3s need not be exact in fp16 (the GEMV path is exact)
+                        // 3-bit levels -4..3 times s: v = level * s is exact in fp32; hi = fp16(v)
+                        // and lo = v - hi (exact in fp16) go to the hi and lo panels
                         const float sf = __half2float(sc);
+                        const uint32_t at_lo = smem_u32(sb + (NA + m) * C::A_BYTES);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            uint32_t qv[4];
+                            uint32_t qv[4], lv[4];
 #pragma unroll
                             for (int h2 = 0; h2 < 4; ++h2) {
-                                __half hv[2];
+                                __half hv[2], lo[2];
 #pragma unroll
                                 for (int u = 0; u < 2; ++u) {
                                     const int i = 8 * c + 2 * h2 + u, off = 3 * i, wi = off >> 5, sh = off & 31;
-                                    const uint32_t lo = cw[m][b][wi];
-                                    const uint32_t hi = wi + 1 < BITS ? cw[m][b][wi + 1] : 0u;
-                                    const int code = (int)(__funnelshift_r(lo, hi, sh) & 7u);
-                                    hv[u] = __float2half_rn((float)(code - 4) * sf);
+                                    const uint32_t lo_w = cw[m][b][wi];
+                                    const uint32_t hi_w = wi + 1 < BITS ? cw[m][b][wi + 1] : 0u;
+                                    const int code = (int)(__funnelshift_r(lo_w, hi_w, sh) & 7u);
+                                    const float v = (float)(code - 4) * sf;
+                                    hv[u] = __float2half_rn(v);
+                                    lo[u] = __float2half_rn(v - __half2float(hv[u]));
                                 }
                                 qv[h2] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+                                lv[h2] = (uint32_t)__half_as_ushort(lo[0]) | ((uint32_t)__half_as_ushort(lo[1]) << 16);
                             }
+                            st_shared_v4(at_lo + sw128_off(r, 4 * b + c), lv[0], lv[1], lv[2], lv[3]);
                             st_shared_v4(at + sw128_off(r, 4 * b + c), qv[0], qv[1], qv[2], qv[3]);
                         }
                     }

@@ -13,7 +13,9 @@ the GEMV path forms G and U from exact integer block dots with fp32 FMAs
 path accumulates 2 * H / 16 = 256 MMAs of K = 16 in the fp32 TMEM accumulator,
 which rounds toward zero at each step: relative error up to 256 * 2^-24 per
 accumulator (~1.5e-5, measured 2.7e-5 on G*U), i.e. |dh/s| up to 127 * 3e-5
-~ 4e-3.
+~ 4e-3.  With 3-bit weights the tensor-core path splits the weight panel into
+fp16 hi + lo as well and spends 3 MMAs per product (384 per accumulator), so
+its bound grows by 3/2 to ~6e-3.
 """
 import numpy as np
 import pytest
@@ -28,6 +30,7 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3
 W_REL = 1e-5
 DELTA = {1: 1e-3, 2: 4e-3}  # GEMV, tensor-core GEMM
+DELTA3 = {1: 1e-3, 2: 6e-3}  # the same with 3-bit weights
 
 
 def _w_close(w_dev, w_ref):
@@ -82,6 +85,16 @@ def full(cuda_lib):
 @pytest.fixture(scope="module")
 def full_skew(cuda_lib):
     return LayerCase(synth.FULL, seed=2, skew=True, device="cuda")
+
+
+@pytest.fixture(scope="module")
+def tiny3(cuda_lib):
+    return LayerCase(synth.LayerShape(H=256, I=128, E=16, k=2, bits=3), seed=3, device="cpu")
+
+
+@pytest.fixture(scope="module")
+def full3(cuda_lib):
+    return LayerCase(synth.FULL3, seed=1, device="cuda")
 
 
 def _ws(moeq, T, shape):
@@ -205,6 +218,51 @@ def test_expert_ffn_full_sampled(full_skew, cuda_lib, mode):
     inv = perm["inv"].cpu().numpy()[tokens]
     _check_h_codes(ref, out["qh"].cpu().numpy(), out["sh"].cpu().numpy(), inv, DELTA[mode])
     full_skew.check_y(out["y"].cpu().numpy()[tokens], ref, delta=DELTA[mode])
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_expert_ffn_tiny_3bit(tiny3, cuda_lib, mode):
+    T = 600
+    x, idx, w, perm, out = _expert_case(tiny3, cuda_lib, T, mode)
+    ref = tiny3.oracle(x)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    _check_h_codes(ref, out["qh"].cpu().numpy(), out["sh"].cpu().numpy(), perm["inv"].cpu().numpy(), DELTA3[mode])
+    tiny3.check_y(out["y"].cpu().numpy(), ref, delta=DELTA3[mode])
+
+
+@pytest.mark.parametrize("T,mode", [(8, 1), (1024, 2)])
+def test_expert_ffn_full_3bit(full3, cuda_lib, T, mode):
+    x, idx, w, perm, out = _expert_case(full3, cuda_lib, T, mode, seed=11)
+    tokens = np.arange(T, dtype=np.int32) if T <= 8 else \
+        np.random.default_rng(2).choice(T, 48, replace=False).astype(np.int32)
+    ref = full3.oracle(x, tokens=tokens)
+    assert np.array_equal(idx.cpu().numpy()[tokens], ref["idx"])
+    inv = perm["inv"].cpu().numpy()[tokens]
+    _check_h_codes(ref, out["qh"].cpu().numpy(), out["sh"].cpu().numpy(), inv, DELTA3[mode])
+    full3.check_y(out["y"].cpu().numpy()[tokens], ref, delta=DELTA3[mode])
+
+
+def test_prefill_experts_repeatable(full_skew, cuda_lib):
+    """Repeated prefill expert calls on the same inputs give bit-identical SwiGLU
+    codes, scales and per-pair outputs (y itself sums the k pairs of a token with
+    fp32 atomics, whose order may vary)."""
+    T = 4096
+    x = full_skew.x(T, seed=7).to(_dev())
+    ws = _ws(cuda_lib, T, full_skew.shape)
+    idx, w = cuda_lib.route_topk(x, full_skew.dev.Wr, full_skew.dev.bias, full_skew.shape.k, ws)
+    perm = cuda_lib.permute(idx, full_skew.shape.E, ws)
+    first = None
+    for _ in range(4):
+        out = cuda_lib.expert_ffn(x, full_skew.W, full_skew.shape.k, perm, w, want_y=True, want_sorted=True,
+                                  mode=2, want_h=True, ws=ws)
+        torch.cuda.synchronize()
+        cur = [out[n].cpu().numpy() for n in ("qh", "sh", "out_sorted")]
+        if first is None:
+            first = cur
+            continue
+        for a, b in zip(first, cur):
+            assert np.array_equal(a, b)
+    assert cuda_lib.device_status() == 0
 
 
 # -------------------------------------------------------------- whole layer
