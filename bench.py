@@ -40,6 +40,9 @@ N_LAYERS = 48
 DECODE_T = 1
 PREFILL_T = 4096
 EXPERT_BYTES = 3 * I * (H // 32) * (8 + 2)  # 2-bit codes + fp16 scales of gate, up, down = 983,040
+EXPERT_BYTES3 = 3 * I * (H // 32) * (12 + 2)  # 3-bit: 1,376,256
+VERIFY_T = 64  # 3-bit decode: a multi-token verify window
+PREFILL3_T = 16384  # 3-bit prefill chunk, uniform routing
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that ncu
 # measured for the current kernel versions on this workload (cold caches): the
 # decode expert kernel (10 experts, T=1) and the prefill gate/up GEMM
@@ -363,6 +366,47 @@ def run_ours(args):
                      d2h_bytes_per_step=Tp * H * 4),
             gpu_launches_per_chunk=PREFILL_LAUNCHES)
 
+    # ---- 3-bit weights: a 64-token verify window (decode path) and a 16,384-token
+    # prefill chunk, one layer with uniform routing (no bias)
+    bits3 = None
+    if not args.no_3bit:
+        l3 = synth.make_layer(synth.FULL3, seed=0, layer=2000, device=dev)
+        W3 = moeq.ExpertWeights.from_layer(l3)
+        torch.cuda.synchronize()
+        res3 = {}
+        for name, T3 in (("decode", VERIFY_T), ("prefill", PREFILL3_T)):
+            ws3 = moeq.workspace(T3, H, I, E, K_TOP, bits=3, device=dev)
+            x3 = synth.make_x(T3, H, seed=31 + rank, device=dev)
+            y3 = torch.empty(T3, H, device=dev)
+            _, idx3, _ = moeq.layer_forward(x3, W3, l3.Wr, None, K_TOP, ws3, y=y3, want_routing=True)
+            torch.cuda.synchronize()
+            g3 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g3):
+                moeq.layer_forward(x3, W3, l3.Wr, None, K_TOP, ws3, y=y3)
+            n3 = max(3, args.steps // 2)
+            t3 = aggregate(T3 * n3, timed(g3.replay, n3, args.warmup), world)
+            sec = t3["seconds"] / n3
+            if name == "decode":
+                uniq = len(set(idx3.flatten().tolist()))
+                nbytes = E * H * 4 + uniq * EXPERT_BYTES3 + 2 * T3 * H * 4
+                ach = nbytes / sec / 1e9
+                roof = dict(bound="hbm", achieved=ach, peak=pk["hbm"], unit="GB/s", frac=ach / pk["hbm"],
+                            traffic=None, kernel="whole layer call (router + expert kernels)",
+                            bytes_per_launch=nbytes, distinct_experts=uniq,
+                            peak_source=f"{pk['source']} hbm_gbs (copy)")
+            else:
+                flop = 2.0 * T3 * K_TOP * 3 * H * I
+                ach = flop / sec / 1e12
+                roof = dict(bound="tensor", achieved=ach, peak=pk["bf16"], unit="TFLOP/s", frac=ach / pk["bf16"],
+                            traffic=None, kernel="whole layer call (router, permutation, both GEMMs)",
+                            flop_per_launch=flop, peak_source=f"{pk['source']} bf16_tflops (burst)")
+            res3[name] = dict(T=T3, value=t3["value"], unit="tokens/s", ms_per_call=1e3 * sec, roofline=roof)
+            del ws3, x3, y3, g3
+        bits3 = dict(workload="3-bit block-32 weights, one 2048/512/512 top-10 layer, uniform routing",
+                     dtype="3-bit x int8 block dots (decode); fp16 tensor-core products of exact hi/lo operands (prefill)",
+                     **res3)
+        del l3, W3
+
     status = moeq.device_status()
     if status:
         raise SystemExit(f"device status 0x{status:x}")
@@ -387,7 +431,7 @@ def run_ours(args):
                     parallelism=f"replicas x{world}"),
         roofline=roof_dec, cpu_baseline=cpu,
         e2e=dict(value=dec_e2e["value"], unit="tokens/s", h2d_bytes_per_step=T * H * 4, d2h_bytes_per_step=T * H * 4),
-        gpu_launches=launches_per_step * args.steps, clocks=clocks, prefill=out or None)
+        gpu_launches=launches_per_step * args.steps, clocks=clocks, prefill=out or None, bits3=bits3)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -406,6 +450,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-3bit", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
