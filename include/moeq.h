@@ -171,6 +171,26 @@ int moe_expert_ffn_q2(const float *x, int T, const moe_qweights *weights, int k,
                       size_t ws_bytes, void *stream);
 
 /*
+ * A shared expert ("Strata — the details", How it works: the shared experts
+ * stay on the GPU beside the routers): one dense SwiGLU expert that every
+ * token passes through, added to the layer output with weight 1 (the pages do
+ * not state a gate, so none is applied).
+ *   y[t] = (accumulate ? y[t] : 0) + W_down h_q(t),  h = silu(W_gate x_q) * (W_up x_q)
+ * with the same block formats and rounding rules as moe_expert_ffn_q2; in fact
+ * it is moe_expert_ffn_q2 with E = 1, k = 1 and every routing weight 1.
+ * shared: E = 1, its own H and I (I a multiple of 128).  x [T,H], y [T,H]
+ * fp32 device arrays, 16-byte aligned; y is read only when accumulate != 0
+ * (call it after moe_layer_forward with accumulate = 1 to add the shared
+ * expert to the routed mixture).  ws: moe_workspace_bytes(T, H, I, 1, 1, bits)
+ * bytes.  mode: MOEQ_MODE_*.  The additions into y are fp32 atomics.
+ * Errors: MOEQ_ERR_ARG (NULL pointer, E != 1, bad mode), MOEQ_ERR_SHAPE,
+ * MOEQ_ERR_ALIGN, MOEQ_ERR_WORKSPACE, MOEQ_ERR_CUDA; nothing is launched on an
+ * argument error.
+ */
+int moe_shared_expert_q2(const float *x, int T, const moe_qweights *shared, float *y, int accumulate, int mode,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Weighted gather-combine: y[t,:] = (residual_x ? residual_x[t,:] : 0)
  *                                  + sum_{j=0..k-1} w[t,j] out_sorted[inv[t,j],:]
  * summed in j order in fp32 (deterministic).  out_sorted [T*k,H], inv [T,k],

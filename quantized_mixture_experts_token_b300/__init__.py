@@ -24,7 +24,8 @@ STATUS_WAIT_TIMEOUT, STATUS_BAD_INDEX = 0x1, 0x2
 
 # Function names of the C ABI (include/moeq.h).
 ABI_FUNCTIONS = (
-    "moe_route_topk", "moe_permute", "moe_permute_noalloc", "moe_quantize_act", "moe_expert_ffn_q2", "moe_combine",
+    "moe_route_topk", "moe_permute", "moe_permute_noalloc", "moe_quantize_act", "moe_expert_ffn_q2",
+    "moe_shared_expert_q2", "moe_combine",
     "moe_layer_forward", "moe_workspace_bytes", "moe_get_device_status", "moe_last_error_string",
     "moe_trace_events", "moe_version",
 )
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.moe_quantize_act.argtypes = [P, i, i, P, P, P]
         L.moe_expert_ffn_q2.argtypes = [P, i, ctypes.POINTER(QWeights), i, P, P, P, P, P, P, i, i, P, P, P, sz, P]
         L.moe_combine.argtypes = [P, P, P, i, i, i, P, P, P]
+        L.moe_shared_expert_q2.argtypes = [P, i, ctypes.POINTER(QWeights), P, i, i, P, sz, P]
         L.moe_layer_forward.argtypes = [P, i, P, P, ctypes.POINTER(QWeights), i, i, P, P, P, i, P, sz, P]
         L.moe_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.moe_workspace_bytes.restype = sz
@@ -209,6 +211,21 @@ def expert_ffn(x, weights: ExpertWeights, k, perm, w=None, *, want_y=True, want_
     if want_h:
         out["qh"], out["sh"] = qh[:P], sh[:P]
     return out
+
+
+def shared_expert(x, weights: ExpertWeights, y=None, *, accumulate=False, mode=MODE_AUTO, ws=None):
+    """y = (y if accumulate else 0) + the shared (E = 1) expert's SwiGLU FFN of every token."""
+    T = x.shape[0]
+    if y is None:
+        if accumulate:
+            raise ValueError("accumulate needs y")
+        y = torch.empty(T, weights.H, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(T, weights.H, weights.I, 1, 1, weights.bits, device=x.device)
+    q = weights.struct()
+    _check(lib().moe_shared_expert_q2(_ptr(x), T, ctypes.byref(q), _ptr(y), int(accumulate), mode, _ptr(ws),
+                                      ws.numel(), _stream(x.device)))
+    return y
 
 
 def combine(out_sorted, inv, w, residual_x=None):

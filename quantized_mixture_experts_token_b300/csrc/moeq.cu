@@ -383,12 +383,12 @@ int permute_multi(const int32_t *idx, int T, int k, int E, int32_t *counts, int3
 // Experts over an existing permutation.
 int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t *offsets, const int32_t *perm_tok,
             const int32_t *perm_slot, const float *w, float *out_sorted, float *y, int residual, int mode,
-            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, cudaStream_t s) {
+            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, cudaStream_t s, bool init_y = true) {
     const int H = wq->H, I = wq->I, E = wq->E, bits = wq->bits;
     const long long P = (long long)T * k;
     if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
     int *ctrl = at<int>(ws, L.ctrl);
-    if (y) {
+    if (y && init_y) {
         const size_t n = (size_t)T * H;
         const int blocks = (int)std::min<size_t>((n / 4 + 255) / 256, 148 * 16);
         if (blocks > 0) init_y_kernel<<<blocks, 256, 0, s>>>(x, y, n, residual);
@@ -640,6 +640,34 @@ int moe_expert_ffn_q2(const float *x, int T, const moe_qweights *weights, int k,
     if (int rc = check_ws(ws, ws_bytes, L)) return rc;
     if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, out_sorted, y, residual, mode, qh_out,
                          sh_out, ws, L, (cudaStream_t)stream))
+        return rc;
+    return ok();
+}
+
+int moe_shared_expert_q2(const float *x, int T, const moe_qweights *shared, float *y, int accumulate, int mode,
+                         void *ws, size_t ws_bytes, void *stream) {
+    if (!shared) return fail(MOEQ_ERR_ARG, "shared is NULL");
+    const int H = shared->H, I = shared->I;
+    if (shared->E != 1) return fail(MOEQ_ERR_ARG, "a shared expert is one expert (E = %d)", shared->E);
+    if (int rc = check_shape(T, H, I, 1, 1)) return rc;
+    if (int rc = check_weights(shared, H, I, 1)) return rc;
+    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
+    if (T > 0) {
+        REQ_PTR(x);
+        REQ_PTR(y);
+    }
+    const Layout L = layout(T, H, I, 1, 1);
+    if (int rc = check_ws(ws, ws_bytes, L)) return rc;
+    if (T == 0) return ok();
+    const cudaStream_t s = (cudaStream_t)stream;
+    int32_t *offsets = at<int32_t>(ws, L.offsets), *perm_tok = at<int32_t>(ws, L.perm_tok);
+    int32_t *perm_slot = at<int32_t>(ws, L.perm_slot);
+    float *w = at<float>(ws, L.w);
+    const unsigned blocks = (unsigned)std::min<long long>((T + 255) / 256, (long long)sm_count() * 4);
+    shared_plan_kernel<<<blocks, 256, 0, s>>>(T, offsets, perm_tok, perm_slot, w);
+    if (int rc = cuda_check("shared_plan_kernel")) return rc;
+    if (int rc = experts(x, T, shared, 1, offsets, perm_tok, perm_slot, w, nullptr, y, 0, mode, nullptr, nullptr, ws,
+                         L, s, /*init_y=*/accumulate == 0))
         return rc;
     return ok();
 }

@@ -197,4 +197,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     }
 }
 
+// The trivial routing of a shared expert: every token is pair t of the single
+// expert 0 with weight 1 (offsets {0, T}, perm_tok = identity, perm_slot = 0).
+__global__ void shared_plan_kernel(int T, int32_t *__restrict__ offsets, int32_t *__restrict__ perm_tok,
+                                   int32_t *__restrict__ perm_slot, float *__restrict__ w) {
+    const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i0 == 0) {
+        offsets[0] = 0;
+        offsets[1] = T;
+    }
+    for (int t = i0; t < T; t += gridDim.x * blockDim.x) {
+        perm_tok[t] = t;
+        perm_slot[t] = 0;
+        w[t] = 1.0f;
+    }
+}
+
 }  // namespace moeq

@@ -97,6 +97,16 @@ def full3(cuda_lib):
     return LayerCase(synth.FULL3, seed=1, device="cuda")
 
 
+@pytest.fixture(scope="module")
+def shared_tiny(cuda_lib):
+    return LayerCase(synth.LayerShape(H=256, I=128, E=1, k=1), seed=6, device="cpu")
+
+
+@pytest.fixture(scope="module")
+def shared_full(cuda_lib):
+    return LayerCase(synth.LayerShape(H=2048, I=512, E=1, k=1), seed=8, device="cuda")
+
+
 def _ws(moeq, T, shape):
     return moeq.workspace(T, shape.H, shape.I, shape.E, shape.k, shape.bits, device=_dev())
 
@@ -240,6 +250,42 @@ def test_expert_ffn_full_3bit(full3, cuda_lib, T, mode):
     inv = perm["inv"].cpu().numpy()[tokens]
     _check_h_codes(ref, out["qh"].cpu().numpy(), out["sh"].cpu().numpy(), inv, DELTA3[mode])
     full3.check_y(out["y"].cpu().numpy()[tokens], ref, delta=DELTA3[mode])
+
+
+def _shared_case(case, cuda_lib, T, mode, tokens=None):
+    """The shared expert through moe_shared_expert_q2, fresh and accumulated onto y0,
+    against the oracle's single-expert layer (E = 1, k = 1: weight 1 for every token)."""
+    x = case.x(T, seed=40 + T, margin=False)
+    xd = x.to(_dev())
+    y = cuda_lib.shared_expert(xd, case.W, mode=mode)
+    y0 = synth.make_x(T, case.shape.H, seed=50 + T).to(_dev())
+    y_acc = cuda_lib.shared_expert(xd, case.W, y=y0.clone(), accumulate=True, mode=mode)
+    torch.cuda.synchronize()
+    ref = case.oracle(x, tokens=tokens)
+    rows = slice(None) if tokens is None else tokens
+    yh = y.cpu().numpy()
+    case.check_y(yh[rows], ref, delta=DELTA[mode])
+    # accumulate adds the same values onto y0 (fp32 atomics: one rounding per addition)
+    added = (y_acc - y0).cpu().numpy()
+    scale = float(np.abs(y0.cpu().numpy()).max() + np.abs(yh).max())
+    assert np.abs(added - yh).max() <= 1e-5 * scale
+    assert cuda_lib.device_status() == 0
+
+
+@pytest.mark.parametrize("T,mode", [(5, 1), (64, 1), (600, 2)])
+def test_shared_expert_tiny(shared_tiny, cuda_lib, T, mode):
+    _shared_case(shared_tiny, cuda_lib, T, mode)
+
+
+@pytest.mark.parametrize("T,mode", [(8, 1), (1024, 2)])
+def test_shared_expert_full(shared_full, cuda_lib, T, mode):
+    tokens = None if T <= 8 else np.random.default_rng(3).choice(T, 48, replace=False).astype(np.int32)
+    _shared_case(shared_full, cuda_lib, T, mode, tokens)
+
+
+def test_shared_expert_rejects_routed_weights(full, cuda_lib):
+    with pytest.raises(cuda_lib.MoeqError):
+        cuda_lib.shared_expert(torch.zeros(4, 2048, device=_dev()), full.W)
 
 
 def test_prefill_experts_repeatable(full_skew, cuda_lib):

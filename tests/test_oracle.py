@@ -295,6 +295,26 @@ def test_layer_zero_input_and_one_expert():
     assert np.array_equal(out["y"], out["D"][:, 0, :].astype(np.float32))
 
 
+def test_layer_single_expert_is_a_dense_expert():
+    # E = 1, k = 1 (the form a shared expert takes): every token goes to expert 0
+    # with weight exactly 1, and y is that expert's down projection, which equals
+    # the dense fp64 SwiGLU of the dequantised matrices up to the int8 rounding of h
+    shape = synth.LayerShape(H=64, I=32, E=1, k=1)
+    ln = synth.make_layer(shape, seed=9).numpy()
+    x = synth.make_x(4, 64, seed=9).numpy()
+    out = oracle.layer(x, ln[0], None, ln[2], ln[3], 2, 1, detail=True)
+    assert (out["idx"] == 0).all() and (out["w"] == 1.0).all()
+    assert np.array_equal(out["y"], out["D"][:, 0, :].astype(np.float32))
+    Wg, Wu, Wd = (oracle.dequantize_matrix(ln[2][m][0], ln[3][m][0], 2, *dims)
+                  for m, dims in enumerate(((32, 64), (32, 64), (64, 32))))
+    q, s = oracle.quantize_block32(x)
+    xq = q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)
+    G, U = xq @ Wg.T, xq @ Wu.T
+    h = G * expit(G) * U
+    dense = h @ Wd.T
+    assert np.abs(out["y"] - dense).max() <= 0.02 * np.abs(dense).max()
+
+
 def test_layer_k_equals_E_is_dense_mixture():
     shape = synth.LayerShape(H=64, I=32, E=4, k=4)
     ln = synth.make_layer(shape, seed=9).numpy()
