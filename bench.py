@@ -43,6 +43,7 @@ EXPERT_BYTES = 3 * I * (H // 32) * (8 + 2)  # 2-bit codes + fp16 scales of gate,
 EXPERT_BYTES3 = 3 * I * (H // 32) * (12 + 2)  # 3-bit: 1,376,256
 VERIFY_T = 64  # 3-bit decode: a multi-token verify window
 PREFILL3_T = 16384  # 3-bit prefill chunk, uniform routing
+SWEEP_T = (8, 16, 32, 64, 128, 256, 512, 1024)  # token counts of the GEMV / grouped-GEMM crossover sweep
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that ncu
 # measured for the current kernel versions on this workload (cold caches): the
 # decode expert kernel (10 experts, T=1) and the prefill gate/up GEMM
@@ -407,6 +408,34 @@ def run_ours(args):
                      **res3)
         del l3, W3
 
+    # ---- expert-path crossover: whole-layer time per call in GEMV and in grouped-GEMM
+    # mode for small T, each replay running all nl resident layers so the selected
+    # experts come from HBM, not L2
+    sweep = None
+    if not args.no_sweep:
+        sweep = []
+        for Ts in SWEEP_T:
+            wss = moeq.workspace(Ts, H, I, E, K_TOP, device=dev)
+            xsw = synth.make_x(Ts, H, seed=61 + Ts, device=dev)
+            ysw = torch.empty(Ts, H, device=dev)
+            row = dict(T=Ts)
+            for mname, mode in (("gemv", moeq.MODE_GEMV), ("gemm", moeq.MODE_GEMM)):
+                def stack(mode=mode):
+                    for l in range(nl):
+                        moeq.layer_forward(xsw, Ws[l], layers[l].Wr, None, K_TOP, wss, y=ysw, mode=mode)
+
+                stack()
+                torch.cuda.synchronize()
+                gs = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs):
+                    stack()
+                nrep = 5
+                row[mname + "_us_per_layer"] = 1e6 * timed(gs.replay, nrep, args.warmup) / (nrep * nl)
+                del gs
+            row["faster"] = "gemv" if row["gemv_us_per_layer"] <= row["gemm_us_per_layer"] else "gemm"
+            sweep.append(row)
+            del wss, xsw, ysw
+
     status = moeq.device_status()
     if status:
         raise SystemExit(f"device status 0x{status:x}")
@@ -431,7 +460,8 @@ def run_ours(args):
                     parallelism=f"replicas x{world}"),
         roofline=roof_dec, cpu_baseline=cpu,
         e2e=dict(value=dec_e2e["value"], unit="tokens/s", h2d_bytes_per_step=T * H * 4, d2h_bytes_per_step=T * H * 4),
-        gpu_launches=launches_per_step * args.steps, clocks=clocks, prefill=out or None, bits3=bits3)
+        gpu_launches=launches_per_step * args.steps, clocks=clocks, prefill=out or None, bits3=bits3,
+        mode_sweep=sweep)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -451,6 +481,7 @@ def main(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-3bit", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

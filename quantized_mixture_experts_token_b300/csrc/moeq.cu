@@ -71,8 +71,13 @@ int cuda_check(const char *what) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Token count up to which the routed experts run as GEMVs (auto mode).
-constexpr int kGemvMaxT = 64;
+// Token count up to which the router logits come from the GEMV router kernel.
+constexpr int kRouteGemvMaxT = 64;
+// Token count up to which auto mode runs the routed experts as GEMVs: measured
+// on B300 (2048/512/512, top-10, 2-bit, experts read from HBM), the GEMV path
+// took 39 / 108 / 181 / 432 / 552 us per layer at T = 8 / 32 / 64 / 128 / 256
+// against 177 / 421 / 614 / 951 / 1004 us for the grouped GEMM.
+constexpr int kExpertGemvMaxT = 256;
 // Token count up to which the decode fast path fuses routing and permutation.
 constexpr int kFusedRouteMaxT = kFusedMaxT;  // (the router kernel's tail handles up to 64 tokens)
 // Token count up to which every expert CTA ranks the router logits itself.
@@ -246,7 +251,7 @@ int route_gemv_dispatch(const float *x, int T, int H, const float *Wr, const flo
 // Router logits + top-k (unfused).
 int route_unfused(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k, int32_t *idx,
                   float *w, float *logits, cudaStream_t s) {
-    if (T <= kGemvMaxT) {
+    if (T <= kRouteGemvMaxT) {
         DecodeTail none{};
         if (int rc = route_gemv_dispatch(x, T, H, Wr, bias, E, logits, none, s)) return rc;
     } else {
@@ -386,7 +391,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
             int8_t *qh_out, float *sh_out, void *ws, const Layout &L, cudaStream_t s, bool init_y = true) {
     const int H = wq->H, I = wq->I, E = wq->E, bits = wq->bits;
     const long long P = (long long)T * k;
-    if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
+    if (mode == MOEQ_MODE_AUTO) mode = T <= kExpertGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
     int *ctrl = at<int>(ws, L.ctrl);
     if (y && init_y) {
         const size_t n = (size_t)T * H;
@@ -712,7 +717,7 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
     int32_t *counts = at<int32_t>(ws, L.counts), *offsets = at<int32_t>(ws, L.offsets);
     int32_t *perm_tok = at<int32_t>(ws, L.perm_tok), *perm_slot = at<int32_t>(ws, L.perm_slot);
     int32_t *inv = at<int32_t>(ws, L.inv);
-    if (mode == MOEQ_MODE_AUTO) mode = T <= kGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
+    if (mode == MOEQ_MODE_AUTO) mode = T <= kExpertGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
     if (T <= kFusedRouteMaxT && mode == MOEQ_MODE_GEMV) {
         // decode: two kernels chained by programmatic dependent launch.  The
         // router kernel also sets y = residual ? x : 0 and quantises x.  For

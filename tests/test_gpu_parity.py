@@ -330,6 +330,20 @@ def test_layer_forward_decode_full(full, cuda_lib, T):
     assert np.abs(y2.cpu().numpy() - y.cpu().numpy()).max() <= 1e-6 * float(y.abs().max())
 
 
+def test_layer_forward_auto_mid_size(full, cuda_lib):
+    """A 200-token call in auto mode (the GEMV expert path above the fused decode range)."""
+    T = 200
+    x = full.x(T, seed=300)
+    ws = _ws(cuda_lib, T, full.shape)
+    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), full.W, full.dev.Wr, None, full.shape.k, ws, want_routing=True)
+    torch.cuda.synchronize()
+    tokens = np.random.default_rng(4).choice(T, 48, replace=False).astype(np.int32)
+    ref = full.oracle(x, tokens=tokens)
+    assert np.array_equal(idx.cpu().numpy()[tokens], ref["idx"])
+    full.check_y(y.cpu().numpy()[tokens], ref, delta=DELTA[1])
+    assert cuda_lib.device_status() == 0
+
+
 @pytest.mark.parametrize("residual", [False, True])
 def test_layer_forward_prefill_full(full_skew, cuda_lib, residual):
     T = 4096
