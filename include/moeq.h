@@ -66,7 +66,7 @@ extern "C" {
 #define MOEQ_STATUS_WAIT_TIMEOUT 0x1 /* a bounded device wait gave up */
 #define MOEQ_STATUS_BAD_INDEX 0x2    /* an expert index outside [0, E) reached a kernel */
 
-#define MOEQ_MODE_AUTO 0 /* GEMV for T <= 256 (faster there on B300), grouped GEMM otherwise */
+#define MOEQ_MODE_AUTO 0 /* GEMV for T <= 512 (faster there on B300), grouped GEMM otherwise */
 #define MOEQ_MODE_GEMV 1 /* per-expert split GEMV with fused SwiGLU/down/combine */
 #define MOEQ_MODE_GEMM 2 /* grouped tcgen05 tensor-core GEMMs */
 

@@ -75,9 +75,9 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 constexpr int kRouteGemvMaxT = 64;
 // Token count up to which auto mode runs the routed experts as GEMVs: measured
 // on B300 (2048/512/512, top-10, 2-bit, experts read from HBM), the GEMV path
-// took 39 / 108 / 181 / 432 / 552 us per layer at T = 8 / 32 / 64 / 128 / 256
-// against 177 / 421 / 614 / 951 / 1004 us for the grouped GEMM.
-constexpr int kExpertGemvMaxT = 256;
+// took 39 / 181 / 552 / 766 / 1237 us per layer at T = 8 / 64 / 256 / 512 / 1024
+// against 177 / 614 / 1003 / 1029 / 1066 us for the grouped GEMM.
+constexpr int kExpertGemvMaxT = 512;
 // Token count up to which the decode fast path fuses routing and permutation.
 constexpr int kFusedRouteMaxT = kFusedMaxT;  // (the router kernel's tail handles up to 64 tokens)
 // Token count up to which every expert CTA ranks the router logits itself.
