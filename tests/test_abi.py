@@ -82,6 +82,18 @@ def test_argument_errors_are_reported_before_launch(L):
                              None)
     assert rc == -1
     assert L.moe_get_device_status(None, None) == -1
+    # shared expert: routed (E != 1) weights, NULL y, bad mode, small workspace
+    rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), P(256), 0, 0, P(256), 1 << 40, None)
+    assert rc == -1 and b"one expert" in L.moe_last_error_string()
+    q.E = 1
+    rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), None, 0, 0, P(256), 1 << 40, None)
+    assert rc == -1 and b"y is NULL" in L.moe_last_error_string()
+    rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), P(256), 1, 3, P(256), 1 << 40, None)
+    assert rc == -1
+    rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), P(256), 1, 0, P(256), 16, None)
+    assert rc == -4
+    need = L.moe_workspace_bytes(4, 2048, 512, 1, 1, 2)
+    assert 0 < need < moeq.workspace_bytes(4, 2048, 512, 512, 10)
 
 
 def test_binding_refuses_host_tensors():
