@@ -150,7 +150,12 @@ int moe_permute_noalloc(const int32_t *idx, int T, int k, int E, int32_t *counts
 int moe_quantize_act(const float *x, int T, int H, int8_t *q_out, float *s_out, void *stream);
 
 /*
- * The experts: for every sorted pair p (token t = perm_tok[p], expert e with
+ * The experts ("Strata - the details", "How it works": the experts a token
+ * selects run on the GPU; "Speed (measured)", engine 0.1.36: prompt experts on
+ * fused int8 tensor-core kernels, 0.1.13: quantised-activation MMQ kernels
+ * instead of FP16-expanded weights).  The FFN form (SwiGLU) and the 2-bit
+ * block format are not on the pages; they are this library's readings.
+ * For every sorted pair p (token t = perm_tok[p], expert e with
  * offsets[e] <= p < offsets[e+1]):
  *   G = W_gate[e] x_q, U = W_up[e] x_q        (x_q: x quantised as above)
  *   h = silu(G) * U, re-quantised per 32-block along I by the same rule
@@ -164,6 +169,11 @@ int moe_quantize_act(const float *x, int T, int H, int8_t *q_out, float *s_out, 
  * w [T,k] fp32 routing weights (needed when y != NULL).  mode: MOEQ_MODE_*.
  * The order of the k additions into y is unspecified (fp32 atomics);
  * out_sorted, qh and sh do not depend on it.
+ * offsets/perm_tok/perm_slot are moe_permute's outputs (the pair's slot j
+ * picks its weight w[t,j]; inv is not needed here).  offsets that are not an
+ * exclusive prefix sum within [0, T*k], or a token or slot out of range, make
+ * the kernels skip the affected work and raise MOEQ_STATUS_BAD_INDEX instead
+ * of reading or writing out of bounds.
  */
 int moe_expert_ffn_q2(const float *x, int T, const moe_qweights *weights, int k, const int32_t *offsets,
                       const int32_t *perm_tok, const int32_t *perm_slot, const float *w, float *out_sorted,
@@ -191,16 +201,25 @@ int moe_shared_expert_q2(const float *x, int T, const moe_qweights *shared, floa
                          void *ws, size_t ws_bytes, void *stream);
 
 /*
- * Weighted gather-combine: y[t,:] = (residual_x ? residual_x[t,:] : 0)
- *                                  + sum_{j=0..k-1} w[t,j] out_sorted[inv[t,j],:]
+ * Weighted gather-combine (each token's output mixes the k experts it picked,
+ * upstream Strata README, "How does it work?": each word needs only 10 of the
+ * 24,576 experts; the residual add between layers is the stack's, attention
+ * being left out):
+ *   y[t,:] = (residual_x ? residual_x[t,:] : 0)
+ *            + sum_{j=0..k-1} w[t,j] out_sorted[inv[t,j],:]
  * summed in j order in fp32 (deterministic).  out_sorted [T*k,H], inv [T,k],
- * w [T,k], residual_x [T,H] or NULL, y_out [T,H].
+ * w [T,k], residual_x [T,H] or NULL, y_out [T,H]; H a multiple of 4.  Needs no
+ * workspace.  A pair whose inv is outside [0, T*k) (moe_permute writes -1 for
+ * a rejected expert index) adds nothing and raises MOEQ_STATUS_BAD_INDEX.
  */
 int moe_combine(const float *out_sorted, const int32_t *inv, const float *w, int T, int k, int H,
                 const float *residual_x, float *y_out, void *stream);
 
 /*
- * The whole layer: route + top-k, permutation, experts and combine, all on
+ * The whole routed expert-FFN layer as the pages' engine runs it per layer
+ * ("Strata - the details", "How it works": routers on the GPU, then each
+ * token's selected experts; prompt chunks batched per expert, "Speed
+ * (measured)"): route + top-k, permutation, experts and combine, all on
  * `stream` with no host synchronisation.  y_out [T,H] = (residual ? x : 0) +
  * the routed mixture.  idx_out/w_out [T,k] optional (may be NULL).
  * Decode calls (T <= 64 in GEMV mode) run as two kernels chained by
@@ -212,12 +231,30 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
                       int k, int residual, float *y_out, int32_t *idx_out, float *w_out, int mode, void *ws,
                       size_t ws_bytes, void *stream);
 
-/* Bytes of workspace every call above needs for these sizes (0 on bad shapes). */
+/* Bytes of workspace every call above needs for these sizes (0 on bad shapes).
+ * The pages size their prompt-chunk buffers to fit borrowed cache slots
+ * ("Strata - the details", "How it works"); here the caller allocates one
+ * buffer of this size per stream and passes it to every call. */
 size_t moe_workspace_bytes(int T, int H, int I, int E, int k, int bits);
 
-/* Synchronises `stream`, returns in *status_out the MOEQ_STATUS_* bits that
- * kernels on the current device recorded since the last call, and clears them. */
+/* Device-side failure report (the pages' engine ends a stuck request with an
+ * error instead of hanging, "Strata - the details", "Troubleshooting").
+ * Synchronises `stream`, returns in *status_out the MOEQ_STATUS_* bits that
+ * kernels on the current device recorded since the last call, and clears them.
+ * Returns MOEQ_ERR_DEVICE when any bit was set.  After
+ * MOEQ_STATUS_WAIT_TIMEOUT the outputs of the calls since the last check are
+ * unspecified; the workspace stays usable (its counters are re-armed). */
 int moe_get_device_status(void *stream, int *status_out);
+
+/* The bound of every device-side pipeline wait, in nanoseconds, on the current
+ * device (the counterpart of the pages' watchdog, "Strata - the details",
+ * "Troubleshooting": STRATA_WATCHDOG_S ends a request that makes no progress).
+ * 0 restores the default of 2 s; at most 60 s.  A wait that runs out raises
+ * MOEQ_STATUS_WAIT_TIMEOUT, and its kernel drains the copies and tensor-core
+ * operations it issued (bounded separately, 2 s) and returns.  Takes effect
+ * for kernels launched after the call returns; call it with no library work
+ * in flight on the device (it writes device memory synchronously). */
+int moe_set_wait_limit(uint64_t ns);
 
 /* Thread-local text of the last error returned on this thread ("" if none). */
 const char *moe_last_error_string(void);

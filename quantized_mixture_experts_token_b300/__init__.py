@@ -27,7 +27,7 @@ ABI_FUNCTIONS = (
     "moe_route_topk", "moe_permute", "moe_permute_noalloc", "moe_quantize_act", "moe_expert_ffn_q2",
     "moe_shared_expert_q2", "moe_combine",
     "moe_layer_forward", "moe_workspace_bytes", "moe_get_device_status", "moe_last_error_string",
-    "moe_trace_events", "moe_version",
+    "moe_trace_events", "moe_version", "moe_set_wait_limit",
 )
 
 
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
         L.moe_last_error_string.restype = ctypes.c_char_p
         L.moe_version.restype = ctypes.c_char_p
         L.moe_trace_events.argtypes = [P, i]
+        L.moe_set_wait_limit.argtypes = [ctypes.c_uint64]
         for name in ABI_FUNCTIONS:
             if name not in ("moe_workspace_bytes", "moe_last_error_string", "moe_version"):
                 getattr(L, name).restype = i
@@ -263,6 +264,11 @@ def trace_events(events) -> None:
         e.record()  # materialise the underlying cudaEvent_t
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib().moe_trace_events(arr, len(events)))
+
+
+def set_wait_limit(ns: int = 0) -> None:
+    """Bound of the device-side pipeline waits in ns (0: the default, 2 s)."""
+    _check(lib().moe_set_wait_limit(int(ns)))
 
 
 def device_status() -> int:

@@ -44,26 +44,44 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Bound of a pipeline wait (moe_set_wait_limit; 2 s by default).  Read from
+// device memory only after a wait has already spun for a while.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+__device__ uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
+// Bound of the waits that drain a CTA's own copies and MMAs before it exits
+// after an abort: fixed, so that a short pipeline limit never lets a CTA leave
+// with asynchronous copies still landing in its shared memory.
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
-// Bounded wait for the phase with the given parity to complete.  Returns false
-// (and raises the CTA's abort flag) if it did not within the limit, or if
-// another thread of the CTA already aborted (when honour_abort is set).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          bool honour_abort = true) {
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag, bool honour_abort,
+                                          uint64_t limit) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 15u) == 0u) {
             if (honour_abort && *abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit) {
                 set_status(MOEQ_STATUS_WAIT_TIMEOUT);
                 *abort_flag = 1;
                 return false;
             }
         }
     }
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false
+// (and raises the CTA's abort flag) if it did not within the pipeline limit,
+// or if another thread of the CTA already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try(bar, parity)) return true;
+    return mbar_spin(bar, parity, abort_flag, true, *(volatile uint64_t *)&g_wait_limit_ns);
+}
+
+// Wait for copies or MMAs this CTA issued itself (after an abort, before it
+// exits); ignores the abort flag, fixed bound.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    return mbar_spin(bar, parity, abort_flag, false, kDrainLimitNs);
 }
 
 // --------------------------------------------------------- bulk copies

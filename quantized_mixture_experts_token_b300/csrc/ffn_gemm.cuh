@@ -300,9 +300,9 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
         }
         if (!ok && lane == 0) {  // drain the copies still in flight
             for (int g2 = max(0, graw - R); g2 < graw; ++g2)
-                mbar_wait(smem_u32(&raw_full[g2 % R]), (g2 / R) & 1, abort_flag, false);
+                mbar_drain(smem_u32(&raw_full[g2 % R]), (g2 / R) & 1, abort_flag);
             for (int g2 = max(0, gb - S); g2 < gb; ++g2)
-                mbar_wait(smem_u32(&b_full[g2 % S]), (g2 / S) & 1, abort_flag, false);
+                mbar_drain(smem_u32(&b_full[g2 % S]), (g2 / S) & 1, abort_flag);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             }
             // every MMA issued above is complete once this commit lands
             mma_commit(smem_u32(drain));
-            mbar_wait(smem_u32(drain), 0, abort_flag, false);
+            mbar_drain(smem_u32(drain), 0, abort_flag);
         }
         __syncwarp();
     } else if (warp < 6) {
@@ -452,10 +452,18 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             const int buf = j & 1, p0 = tl.p0, nval = tl.n, nround = (nval + 15) & ~15;
             {
                 const int p = p0 + min(et, nval - 1);
-                const int t = a.perm_tok[p];
+                int t = a.perm_tok[p];
+                const int js = a.perm_slot[p];
+                float wv = 0.f;
+                if (t < 0 || t >= a.T || js < 0 || js >= a.k) {  // a caller's bad permutation: no contribution
+                    set_status(MOEQ_STATUS_BAD_INDEX);
+                    t = 0;
+                } else if (!GATEUP && a.w) {
+                    wv = a.w[(size_t)t * a.k + js];
+                }
                 s_tok[buf * kGmN + et] = t;
                 s_exp[buf * kGmN + et] = a.brow_exp[p];
-                s_wt[buf * kGmN + et] = (!GATEUP && a.w) ? a.w[(size_t)t * a.k + a.perm_slot[p]] : 0.f;
+                s_wt[buf * kGmN + et] = wv;
             }
             named_sync(1, 128);
             if (dead) continue;

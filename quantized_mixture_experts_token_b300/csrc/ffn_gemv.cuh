@@ -328,18 +328,22 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
             bulk_g2s(smem_u32(xsum + r * KBH), a.xsum + t * KBH, (uint32_t)(4 * KBH), bar_x, 0);
         }
     };
-    bool x_staged = false;  // route_mode 1: every token staged once, row = token
+    bool x_staged = false;   // route_mode 1: every token staged once, row = token
+    bool x_pending = false;  // a copy into the staging rows is in flight (not yet waited for)
     if (a.route_mode == 1) {
         if (tid == 0) issue_x(true, a.T);
         x_staged = true;
+        x_pending = true;
     }
     int e = 0, pb = 0, ne = 0;
-    if (!gemv_unit<PER>(a, u, tok, wt, e, pb, ne)) return;  // uniform over the CTA
-    if (e < 0 || e >= a.E) {
-        set_status(MOEQ_STATUS_BAD_INDEX);
+    const bool have = gemv_unit<PER>(a, u, tok, wt, e, pb, ne);  // uniform over the CTA
+    const bool bad = have && (e < 0 || e >= a.E);
+    if (!have || bad || ne <= 0) {
+        if (bad && tid == 0) set_status(MOEQ_STATUS_BAD_INDEX);
+        // the CTA's shared memory must not be released while the staging copy lands
+        if (x_pending && tid == 0) mbar_drain(bar_x, 0, abort_flag);
         return;
     }
-    if (ne <= 0) return;
 
     const int ngc = (KBH + a.kc - 1) / a.kc, ndc = (a.H + a.rc - 1) / a.rc;
     const uint64_t pol = l2_evict_first();
@@ -380,14 +384,23 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
         const int nt = min(a.tc, ne - c0);
         if (c0 > 0 && tid < nt) {  // later passes (more than tc tokens): from the permutation arrays
             const int p = pb + c0 + tid;
-            const int t = __ldcg(a.perm_tok + p);
+            int t = __ldcg(a.perm_tok + p);
+            const int j = __ldcg(a.perm_slot + p);
+            float wv = 0.f;
+            if (t < 0 || t >= a.T || j < 0 || j >= a.k) {  // a caller's bad permutation: no contribution
+                set_status(MOEQ_STATUS_BAD_INDEX);
+                t = 0;
+            } else if (a.y) {
+                wv = __ldcg(a.w + (size_t)t * a.k + j);
+            }
             tok[tid] = t;
-            wt[tid] = a.y ? __ldcg(a.w + (size_t)t * a.k + __ldcg(a.perm_slot + p)) : 0.f;
+            wt[tid] = wv;
         }
         __syncthreads();
         // 1. the pass's quantised activations (route_mode 1: staged once for all tokens)
         if (!x_staged) {
             if (tid == 0) issue_x(false, nt);
+            x_pending = true;
             if (tid < nt) xrow[tid] = tid;
         } else if (tid < nt) {
             xrow[tid] = tok[tid];
@@ -399,6 +412,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
                 break;
             }
             ++x_ph;
+            x_pending = false;
             x_ready = x_staged;
         } else {
             __syncthreads();
@@ -514,9 +528,9 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
     }
     if (failed && tid == 0) {
         // drain the copies still in flight before the CTA's shared memory is released
-        if (!gu_ready) mbar_wait(bar_gu, gu_ph & 1, abort_flag, false);
-        if (!d_ready) mbar_wait(bar_d, d_ph & 1, abort_flag, false);
-        if (!x_ready && !x_staged) mbar_wait(bar_x, x_ph & 1, abort_flag, false);
+        if (!gu_ready) mbar_drain(bar_gu, gu_ph & 1, abort_flag);
+        if (!d_ready) mbar_drain(bar_d, d_ph & 1, abort_flag);
+        if (x_pending) mbar_drain(bar_x, x_ph & 1, abort_flag);
     }
 }
 

@@ -399,7 +399,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
         if (blocks > 0) init_y_kernel<<<blocks, 256, 0, s>>>(x, y, n, residual);
     }
     if (T == 0) return cuda_check("init_y_kernel");
-    plan_kernel<<<1, 1024, 0, s>>>(offsets, E, ctrl, mode == MOEQ_MODE_GEMV ? at<UnitRec>(ws, L.units) : nullptr,
+    plan_kernel<<<1, 1024, 0, s>>>(offsets, E, T, ctrl, mode == MOEQ_MODE_GEMV ? at<UnitRec>(ws, L.units) : nullptr,
                                    perm_tok, perm_slot, y ? w : nullptr, k, at<Tile>(ws, L.tiles));
     if (int rc = cuda_check("plan_kernel")) return rc;
     if (mode == MOEQ_MODE_GEMV) {
@@ -449,7 +449,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0);
     if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
     const unsigned split_blocks = (unsigned)std::min<long long>((P + 7) / 8, (long long)sm_count() * 16);
-    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, offsets, E, ximg, img_rows, ex);
+    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, T, offsets, E, ximg, img_rows, ex);
     if (int rc = cuda_check("split_rows_kernel(x)")) return rc;
     const long long max_tiles = (P + kTileN - 1) / kTileN + E;
     GemmArgs g{};
@@ -474,7 +474,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     g.sh = sh;
     int rc = bits == 2 ? launch_gemm<true, 2>(g, max_tiles, s) : launch_gemm<true, 3>(g, max_tiles, s);
     if (rc) return rc;
-    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qh, sh, I, nullptr, (int)P, offsets, E, himg, img_rows, eh);
+    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qh, sh, I, nullptr, (int)P, (int)P, offsets, E, himg, img_rows, eh);
     if ((rc = cuda_check("split_rows_kernel(h)"))) return rc;
     g.bimg = himg;
     g.brow_exp = eh;
@@ -687,7 +687,8 @@ int moe_combine(const float *out_sorted, const int32_t *inv, const float *w, int
     REQ_PTR(w);
     OPT_PTR(residual_x);
     REQ_PTR(y_out);
-    combine_kernel<<<T, 256, 0, (cudaStream_t)stream>>>(out_sorted, inv, w, k, H, residual_x, y_out);
+    combine_kernel<<<T, 256, 0, (cudaStream_t)stream>>>(out_sorted, inv, w, k, H, (long long)T * k, residual_x,
+                                                            y_out);
     if (int rc = cuda_check("combine_kernel")) return rc;
     return ok();
 }
@@ -776,6 +777,15 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
     if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, nullptr, y_out, residual, mode, nullptr,
                          nullptr, ws, L, s))
         return rc;
+    return ok();
+}
+
+int moe_set_wait_limit(uint64_t ns) {
+    constexpr uint64_t kMaxLimitNs = 60ull * 1000000000ull;
+    if (ns > kMaxLimitNs) return fail(MOEQ_ERR_ARG, "wait limit %llu ns above 60 s", (unsigned long long)ns);
+    const uint64_t v = ns ? ns : kDefaultWaitLimitNs;
+    cudaError_t e = cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof v);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "wait limit: %s", cudaGetErrorString(e));
     return ok();
 }
 

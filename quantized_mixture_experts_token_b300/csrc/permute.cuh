@@ -32,9 +32,12 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict
         const int e = idx[p], t = p / k;
         if (e < 0 || e >= E) {
             set_status(MOEQ_STATUS_BAD_INDEX);
+            inv[p] = -1;  // a rejected pair has no sorted position
             continue;
         }
-        atomicOr(&masks[(size_t)e * W + (t >> 5)], 1u << (t & 31));
+        const unsigned bit = 1u << (t & 31);
+        if (atomicOr(&masks[(size_t)e * W + (t >> 5)], bit) & bit)
+            set_status(MOEQ_STATUS_BAD_INDEX);  // the same expert twice in one row
     }
     __syncthreads();
     for (int e = tid; e < E; e += nt) {
@@ -90,7 +93,9 @@ __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t *__res
             set_status(MOEQ_STATUS_BAD_INDEX);
             continue;
         }
-        atomicOr(&s_mask[e * kPermChunkWords + (t >> 5) - w0], 1u << (t & 31));
+        const unsigned bit = 1u << (t & 31);
+        if (atomicOr(&s_mask[e * kPermChunkWords + (t >> 5) - w0], bit) & bit)
+            set_status(MOEQ_STATUS_BAD_INDEX);  // the same expert twice in one row
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -134,7 +139,10 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const int32_t *__r
     const int W = (T + 31) / 32, P = T * k;
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
         const int e = idx[p], t = p / k, j = p - t * k;
-        if (e < 0 || e >= E) continue;
+        if (e < 0 || e >= E) {
+            inv[p] = -1;  // rejected in permute_count_kernel
+            continue;
+        }
         const int w = t >> 5;
         const size_t wi = (size_t)e * W + w;
         const int pos = offsets[e] + chunk_base[(size_t)(w / kPermChunkWords) * E + e] + wprefix[wi] +
@@ -155,20 +163,33 @@ struct Tile {
     int e, p0, n, pad;
 };
 
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int E, int *ctrl,
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int E, int T, int *ctrl,
                                                     UnitRec *units, const int32_t *__restrict__ perm_tok,
                                                     const int32_t *__restrict__ perm_slot,
                                                     const float *__restrict__ w, int k, Tile *tiles) {
     __shared__ int s_act[kMaxE];
     __shared__ int s_til[kMaxE];
     __shared__ int s_scan[33];
+    __shared__ int s_bad;
     const int tid = threadIdx.x;
+    const long long P = (long long)T * k;
+    if (tid == 0) s_bad = (offsets[0] != 0 || offsets[E] < 0 || offsets[E] > P);
+    __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) {
         const int c = offsets[e + 1] - offsets[e];
+        if (c < 0) s_bad = 1;
         s_act[e] = c > 0;
         s_til[e] = (c + kTileN - 1) / kTileN;
     }
     __syncthreads();
+    if (s_bad) {  // offsets that are not a prefix sum over [0, T*k]: no work at all
+        if (tid == 0) {
+            set_status(MOEQ_STATUS_BAD_INDEX);
+            ctrl[1] = 0;
+            ctrl[2] = 0;
+        }
+        return;
+    }
     const int n_active = block_exclusive_scan(s_act, E, s_scan);
     const int n_tiles = block_exclusive_scan(s_til, E, s_scan);
     for (int e = tid; e < E; e += blockDim.x) {
@@ -177,9 +198,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
             UnitRec *r = units + s_act[e];
             *reinterpret_cast<int4 *>(r) = make_int4(e, o, c, 0);
             for (int i = 0; i < min(c, kUnitTok); ++i) {
-                const int t = perm_tok[o + i];
+                int t = perm_tok[o + i];
+                const int j = perm_slot[o + i];
+                float wv = 0.f;
+                if (t < 0 || t >= T || j < 0 || j >= k) {  // no contribution from a bad pair
+                    set_status(MOEQ_STATUS_BAD_INDEX);
+                    t = 0;
+                } else if (w) {
+                    wv = w[(size_t)t * k + j];
+                }
                 r->tok[i] = t;
-                r->w[i] = w ? w[(size_t)t * k + perm_slot[o + i]] : 0.f;
+                r->w[i] = wv;
             }
         }
         for (int i = 0; i * kTileN < c; ++i) {

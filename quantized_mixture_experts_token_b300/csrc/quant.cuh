@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict
 // of each half per lane per step.
 __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restrict__ q, const float *__restrict__ s,
                                                          int n, const int32_t *__restrict__ row_map, int rows,
+                                                         int src_rows,
                                                          const int32_t *__restrict__ offsets, int E,
                                                          __half *__restrict__ img, long long img_rows,
                                                          int *__restrict__ e_out) {
@@ -107,7 +108,12 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restric
             else hi_e = mid;
         }
         const uint32_t phase = (uint32_t)(r - offsets[lo_e]) & 7u;
-        const size_t src = row_map ? (size_t)row_map[r] : (size_t)r;
+        int srow = row_map ? row_map[r] : r;
+        if (srow < 0 || srow >= src_rows) {  // a caller's bad permutation: read row 0 instead
+            if (lane == 0) set_status(MOEQ_STATUS_BAD_INDEX);
+            srow = 0;
+        }
+        const size_t src = (size_t)srow;
         const float *sr = s + src * nb;
         float m = 0.f;
         for (int b = lane; b < nb; b += 32) m = fmaxf(m, sr[b]);

@@ -337,17 +337,17 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
         }
         __syncthreads();
     }
-    if (failed) {
-        if (tid == 0 && !ready) mbar_wait(bar, ph & 1, &s_abort, false);  // drain the copy in flight
-        return;  // the arrival counter is never completed: the call's status word reports the timeout
-    }
+    if (failed && tid == 0 && !ready) mbar_drain(bar, ph & 1, &s_abort);  // the copy in flight lands first
     if (tail.mode < 2) return;
 
     // ---- the last CTA to finish ranks every token and groups the pairs by expert.
     // The barrier orders this CTA's logit and quantisation writes before thread
-    // 0's device-scope fence (cumulative), which precedes its arrival.
+    // 0's device-scope fence (cumulative), which precedes its arrival.  A CTA
+    // whose wait gave up still arrives (after flagging ctrl[3]), so the counter
+    // is always completed and re-armed; the last CTA then publishes no work.
     __syncthreads();
     if (tid == 0) {
+        if (failed) atomicExch(&tail.ctrl[3], 1);
         __threadfence();
         const int prev = atomicAdd(&tail.ctrl[0], 1);
         s_last = (prev == (int)gridDim.x - 1);
@@ -357,6 +357,14 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    if (__ldcg(&tail.ctrl[3])) {  // some CTA's logits are missing: no expert work this call
+        if (tid == 0) {
+            tail.ctrl[1] = 0;
+            tail.ctrl[3] = 0;
+            tail.ctrl[0] = 0;
+        }
+        return;
+    }
 
     int(*s_sel)[kMaxK] = reinterpret_cast<int(*)[kMaxK]>(rsm + L.sel);
     float(*s_selw)[kMaxK] = reinterpret_cast<float(*)[kMaxK]>(rsm + L.selw);

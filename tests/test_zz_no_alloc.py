@@ -27,7 +27,8 @@ def _idx(T, E, k, seed):
     return np.stack([rng.choice(E, k, replace=False, p=use_p) for _ in range(T)]).astype(np.int32)
 
 
-@pytest.mark.parametrize("T,E,k", [(4096, 512, 10), (64, 16, 2), (1, 512, 10)])
+# (2048, 1024, 32): E * ceil(T/32) = 65,536 words, the whole scratch array
+@pytest.mark.parametrize("T,E,k", [(4096, 512, 10), (64, 16, 2), (1, 512, 10), (2048, 1024, 32)])
 def test_noalloc_permute_matches_workspace_permute_twice(cuda_lib, T, E, k):
     dev = torch.device("cuda:0")
     ws = cuda_lib.workspace(T, 128, 128, E, k, device=dev)
@@ -47,3 +48,21 @@ def test_noalloc_permute_rejects_sizes_beyond_its_scratch(cuda_lib):
     rc = L.moe_permute_noalloc(P(256), 4096, 10, 1024, P(256), P(256), P(256), P(256), P(256), None)
     assert rc == -2
     assert b"fixed scratch" in L.moe_last_error_string()
+
+
+def test_noalloc_permute_zero_tokens_zeroes_counts_and_offsets(cuda_lib):
+    dev = torch.device("cuda:0")
+    E, k = 512, 10
+    # fill the outputs with garbage first: a T = 0 call must write zeros
+    idx = torch.zeros(0, k, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        got = cuda_lib.permute_noalloc(idx, E)
+        got["counts"].fill_(7)
+        got["offsets"].fill_(7)
+        L = cuda_lib.lib()
+        P = ctypes.c_void_p
+        rc = L.moe_permute_noalloc(None, 0, k, E, P(got["counts"].data_ptr()), P(got["offsets"].data_ptr()),
+                                   None, None, None, P(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert not got["counts"].any() and not got["offsets"].any()
