@@ -2,17 +2,21 @@
 """Throughput of the routed expert-FFN layer on B300.
 
 Headline workload (one JSON line on stdout, rank 0):
-  decode -- one token (B=1) through a stack of 48 resident MoE layers
-            (H=2048, E=512, I=512, top-10, 2-bit block-32 weights, residual
-            add between layers); `value` is per-layer tokens/s, i.e. tokens
-            through one layer per second, measured over the whole stack so
-            every step reads 48 distinct layers' experts (~673 MB > L2).
-  prefill -- a 4,096-token chunk through one such layer whose router bias is
-            Zipf-skewed (some experts get no token), reported in the "prefill"
-            object (inputs 0.57 GB > L2).
-Both are replayed from CUDA graphs of the library's C-ABI calls.  The
-expert kernels' device time comes from CUDA events the library records
-around them (moe_trace_events); roofline fractions use MEASURED_PEAKS.json.
+  decode  -- one token (B=1) through a stack of 48 resident MoE layers
+             (H=2048, E=512, I=512, top-10, 2-bit block-32 weights, residual
+             add between layers); `value` is per-layer tokens/s, i.e. tokens
+             through one layer per second, measured over the whole stack so
+             every step reads 48 distinct layers' experts (~673 MB > L2).
+Further objects of the same line:
+  decode_t8 -- the same stack at 8 tokens per call (a multi-token decode call)
+  prefill   -- a 4,096-token chunk through one layer whose router bias is
+               Zipf-skewed (some experts get no token; inputs 0.57 GB > L2)
+  stack     -- a 32,768-token prompt as 8 chunks of 4,096 tokens through all
+               48 layers, then 256 decode steps of one token
+  bits3     -- 3-bit weights: a 64-token verify window and a 16,384-token chunk
+  mode_sweep-- GEMV vs grouped-GEMM expert path per call size
+All are replayed from CUDA graphs of the library's C-ABI calls.  Roofline
+fractions use MEASURED_PEAKS.json.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -38,20 +42,21 @@ METRIC = "MoE expert-FFN tokens/s (4K prefill, B=1 decode); % of int8 / HBM roof
 H, I, E, K_TOP = 2048, 512, 512, 10
 N_LAYERS = 48
 DECODE_T = 1
+DECODE_T8 = 8
 PREFILL_T = 4096
+PROMPT_T = 32768  # the stack's prompt, read in PREFILL_T-token chunks
+STACK_DECODE_STEPS = 256
 EXPERT_BYTES = 3 * I * (H // 32) * (8 + 2)  # 2-bit codes + fp16 scales of gate, up, down = 983,040
 EXPERT_BYTES3 = 3 * I * (H // 32) * (12 + 2)  # 3-bit: 1,376,256
+ROUTER_BYTES = E * H * 4  # fp32 router matrix, read once per decode call
 VERIFY_T = 64  # 3-bit decode: a multi-token verify window
 PREFILL3_T = 16384  # 3-bit prefill chunk, uniform routing
 SWEEP_T = (8, 16, 32, 64, 128, 256, 512, 1024)  # token counts of the GEMV / grouped-GEMM crossover sweep
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that ncu
-# measured for the current kernel versions on this workload (cold caches): the
-# decode expert kernel (10 experts, T=1) and the prefill gate/up GEMM
-GEMV_TRAFFIC_BYTES = 9.92e6
-GEMM_GU_TRAFFIC_BYTES = 690.0e6 + 19.6e6
-# library kernels per prefill chunk: router SGEMM, top-k, 3 permutation kernels,
-# plan, y init, x quantisation, 2 operand images, 2 GEMMs
-PREFILL_LAUNCHES = 12
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# current kernel versions from one ncu capture, with its source; None until
+# the kernel in this tree has been captured
+DECODE_LAYER_TRAFFIC = dict(bytes=None, source="not captured for this kernel version")
+GEMM_GU_TRAFFIC = dict(bytes=None, source="not captured for this kernel version")
 
 
 # ------------------------------------------------------------------ helpers
@@ -203,6 +208,280 @@ def run_reference(args):
 # ------------------------------------------------------------ ours (GPU)
 
 
+class Gpu:
+    """Device, library, peaks and the timing helpers shared by the sections."""
+
+    def __init__(self, world, local):
+        import torch
+
+        import quantized_mixture_experts_token_b300 as moeq
+
+        self.torch, self.moeq, self.world = torch, moeq, world
+        self.dev = torch.device("cuda", local)
+        self.pk = peaks()
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    def timed(self, fn, steps, warmup):
+        """Seconds for `steps` calls of fn after `warmup` untimed ones (CUDA events)."""
+        torch = self.torch
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        self.barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        self.barrier()
+        return s.elapsed_time(e) / 1e3
+
+    def graph(self, fn):
+        torch = self.torch
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+
+def s8_peak_tops():
+    """Measured dense int8 throughput of the warp-level mma.sync s8 path (libmoeq_peaks)."""
+    import ctypes
+
+    lib = ctypes.CDLL(os.path.join(ROOT, "quantized_mixture_experts_token_b300", "libmoeq_peaks.so"))
+    lib.moe_peak_mma_s8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    best = 0.0
+    for _ in range(3):
+        v = ctypes.c_double(0.0)
+        if lib.moe_peak_mma_s8(20000, 4, ctypes.byref(v)) == 0:
+            best = max(best, v.value)
+    return best or None
+
+
+def distinct_experts(gpu, xs, Ws, layers, ws, nl):
+    """Distinct experts the tokens of xs[l] select in layer l (read back once)."""
+    out = []
+    for l in range(nl):
+        _, idx, _ = gpu.moeq.layer_forward(xs[l], Ws[l], layers[l].Wr, None, K_TOP, ws, residual=True,
+                                           y=gpu.torch.empty_like(xs[l]), want_routing=True)
+        out.append(len(set(idx.flatten().tolist())))
+    return out
+
+
+def decode_stack(gpu, layers, Ws, T, steps, warmup, seed, clocks=False):
+    """T tokens through the nl-layer stack per step (x_{l+1} = x_l + moe_l(x_l)),
+    one CUDA graph per step; returns timing, bytes and the roofline figures."""
+    torch, moeq = gpu.torch, gpu.moeq
+    nl = len(layers)
+    ws = moeq.workspace(T, H, I, E, K_TOP, device=gpu.dev)
+    xs = [torch.empty(T, H, device=gpu.dev) for _ in range(nl + 1)]
+    import synth
+
+    xs[0].copy_(synth.make_x(T, H, seed=seed, device=gpu.dev))
+
+    def step():
+        for l in range(nl):
+            moeq.layer_forward(xs[l], Ws[l], layers[l].Wr, None, K_TOP, ws, residual=True, y=xs[l + 1])
+
+    g = gpu.graph(step)
+    clk = None
+    if clocks:
+        with ClockSampler(gpu.dev.index) as sampler:
+            t = gpu.timed(g.replay, steps, warmup)
+        clk = sampler.summary()
+    else:
+        t = gpu.timed(g.replay, steps, warmup)
+    agg = aggregate(T * nl * steps, t, gpu.world)
+    uniq = distinct_experts(gpu, xs, Ws, layers, ws, nl)
+    layer_s = agg["seconds"] / (steps * nl)
+    nbytes = ROUTER_BYTES + statistics.mean(uniq) * EXPERT_BYTES + 2 * T * H * 4
+    ach = nbytes / layer_s / 1e9
+    pk = gpu.pk
+    roof = dict(bound="hbm", achieved=ach, peak=pk["hbm"], unit="GB/s", frac=ach / pk["hbm"],
+                traffic=DECODE_LAYER_TRAFFIC["bytes"], traffic_source=DECODE_LAYER_TRAFFIC["source"],
+                kernel="one decode layer: route_gemv_kernel + ffn_gemv_kernel (PDL-chained)",
+                bytes_per_launch=nbytes, distinct_experts=statistics.mean(uniq), launch_us=layer_s * 1e6,
+                frac_of_8tbs=ach / 8000.0, peak_source=f"{pk['source']} hbm_gbs (copy)")
+    return dict(agg=agg, roof=roof, graph=g, xs=xs, ws=ws, clocks=clk, layer_us=layer_s * 1e6)
+
+
+def prefill_chunk(gpu, pre_layer, preW, args, rank):
+    """One 4,096-token chunk through the skewed layer: time, e2e and the
+    per-kernel rooflines (router GEMM, gate/up GEMM, down GEMM)."""
+    torch, moeq = gpu.torch, gpu.moeq
+    import synth
+
+    Tp = PREFILL_T
+    wsp = moeq.workspace(Tp, H, I, E, K_TOP, device=gpu.dev)
+    xp = synth.make_x(Tp, H, seed=21 + rank, device=gpu.dev)
+    yp = torch.empty(Tp, H, device=gpu.dev)
+
+    def call():
+        moeq.layer_forward(xp, preW, pre_layer.Wr, pre_layer.bias, K_TOP, wsp, y=yp)
+
+    g = gpu.graph(call)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    moeq.trace_events(ev)
+    g_tr = gpu.graph(call)
+    moeq.trace_events(None)
+    psteps = max(3, args.steps // 2)
+    t = gpu.timed(g.replay, psteps, args.warmup)
+    pre = aggregate(Tp * psteps, t, gpu.world)
+    for _ in range(3):
+        g_tr.replay()
+    torch.cuda.synchronize()
+    rt_s, gu_s, dn_s = (ev[2 * i].elapsed_time(ev[2 * i + 1]) / 1e3 for i in range(3))
+    P = Tp * K_TOP
+    gu_flop, dn_flop, rt_flop = 2.0 * P * 2 * I * H, 2.0 * P * H * I, 2.0 * Tp * E * H
+    pk = gpu.pk
+    ach = gu_flop / gu_s / 1e12
+    xh = torch.empty(Tp, H, pin_memory=True)
+    xh.copy_(xp.cpu())
+    yh = torch.empty(Tp, H, pin_memory=True)
+
+    def e2e():
+        xp.copy_(xh, non_blocking=True)
+        g.replay()
+        yh.copy_(yp, non_blocking=True)
+
+    pe = aggregate(Tp * psteps, gpu.timed(e2e, psteps, args.warmup), gpu.world)
+    tf32_peak = pk["bf16"] / 2.0  # tf32 dense rate is half the bf16 rate (nominal 1.1 vs 2.25 PFLOP/s)
+    s8 = s8_peak_tops()
+    return dict(
+        value=pre["value"], unit="tokens/s", ms_per_chunk=1e3 * pre["seconds"] / psteps,
+        workload="prefill: 4,096-token chunk through one 2048/512/512 top-10 2-bit layer, Zipf(1.1)-skewed router",
+        dtype=("fp16 tensor-core products of the exact 2-bit levels and an fp16 hi/lo split of the int8 "
+               "activations, fp32 accumulate; router 3xTF32"),
+        roofline=dict(bound="tensor", achieved=ach, peak=pk["bf16"], unit="TFLOP/s", frac=ach / pk["bf16"],
+                      traffic=GEMM_GU_TRAFFIC["bytes"], traffic_source=GEMM_GU_TRAFFIC["source"],
+                      kernel="ffn_gemm_kernel<gate/up>", flop_per_launch=gu_flop, launch_us=gu_s * 1e6,
+                      peak_source=f"{pk['source']} bf16_tflops (burst; fp16 = bf16 rate)",
+                      note="useful FLOP; the exact hi/lo scheme issues two MMAs per product, so 0.5 is its ceiling",
+                      s8_peak=dict(value=s8, unit="TOP/s", source="measured mma.sync m16n8k32 s8 (libmoeq_peaks)",
+                                   frac=(ach / s8) if s8 else None),
+                      down=dict(achieved=dn_flop / dn_s / 1e12, frac=dn_flop / dn_s / 1e12 / pk["bf16"],
+                                launch_us=dn_s * 1e6, flop_per_launch=dn_flop),
+                      router=dict(achieved=rt_flop / rt_s / 1e12, frac_of_tf32=rt_flop / rt_s / 1e12 / tf32_peak,
+                                  launch_us=rt_s * 1e6, flop_per_launch=rt_flop, kernel="route_tc_kernel (3xTF32)",
+                                  peak_source="tf32 = measured bf16 / 2")),
+        e2e=dict(value=pe["value"], unit="tokens/s", h2d_bytes_per_step=Tp * H * 4, d2h_bytes_per_step=Tp * H * 4))
+
+
+def stack_prompt(gpu, layers, Ws, args, rank):
+    """Config of the whole model: a PROMPT_T-token prompt in PREFILL_T-token
+    chunks through every layer of the stack (each chunk one CUDA graph of nl
+    layer calls), then STACK_DECODE_STEPS single-token decode steps."""
+    torch, moeq = gpu.torch, gpu.moeq
+    import synth
+
+    nl = len(layers)
+    n_chunks = PROMPT_T // PREFILL_T
+    wsp = moeq.workspace(PREFILL_T, H, I, E, K_TOP, device=gpu.dev)
+    prompt = synth.make_x(PROMPT_T, H, seed=41 + rank, device=gpu.dev)
+    buf = [torch.empty(PREFILL_T, H, device=gpu.dev) for _ in range(2)]
+
+    def chunk_pass():
+        for l in range(nl):
+            moeq.layer_forward(buf[l & 1], Ws[l], layers[l].Wr, None, K_TOP, wsp, residual=True,
+                               y=buf[(l + 1) & 1])
+
+    g = gpu.graph(chunk_pass)
+
+    def prompt_pass():
+        for c in range(n_chunks):
+            buf[0].copy_(prompt[c * PREFILL_T:(c + 1) * PREFILL_T])
+            g.replay()
+
+    reps = max(1, args.stack_reps)
+    t = gpu.timed(prompt_pass, reps, 1)
+    pre = aggregate(PROMPT_T * reps, t, gpu.world)
+    del g, wsp, buf, prompt
+    torch.cuda.empty_cache()
+    dec = decode_stack(gpu, layers, Ws, 1, STACK_DECODE_STEPS, args.warmup, seed=51 + rank)
+    return dict(
+        workload=(f"{PROMPT_T}-token prompt in {n_chunks} chunks of {PREFILL_T} through {nl} layers "
+                  f"(uniform routing, residual between layers), then {STACK_DECODE_STEPS} decode steps of one token"),
+        prefill=dict(value=pre["value"], unit="prompt tokens/s through the stack",
+                     ms_per_prompt=1e3 * pre["seconds"] / reps, reps=reps),
+        decode=dict(value=dec["agg"]["value"] / nl, unit="tokens/s through the stack",
+                    ms_per_token=1e3 * dec["agg"]["seconds"] / STACK_DECODE_STEPS, steps=STACK_DECODE_STEPS,
+                    roofline_frac=dec["roof"]["frac"]))
+
+
+def bits3_section(gpu, args, rank):
+    torch, moeq = gpu.torch, gpu.moeq
+    import synth
+
+    pk = gpu.pk
+    l3 = synth.make_layer(synth.FULL3, seed=0, layer=2000, device=gpu.dev)
+    W3 = moeq.ExpertWeights.from_layer(l3)
+    torch.cuda.synchronize()
+    res = {}
+    for name, T3 in (("decode", VERIFY_T), ("prefill", PREFILL3_T)):
+        ws3 = moeq.workspace(T3, H, I, E, K_TOP, bits=3, device=gpu.dev)
+        x3 = synth.make_x(T3, H, seed=31 + rank, device=gpu.dev)
+        y3 = torch.empty(T3, H, device=gpu.dev)
+        _, idx3, _ = moeq.layer_forward(x3, W3, l3.Wr, None, K_TOP, ws3, y=y3, want_routing=True)
+        g3 = gpu.graph(lambda: moeq.layer_forward(x3, W3, l3.Wr, None, K_TOP, ws3, y=y3))
+        n3 = max(3, args.steps // 2)
+        t3 = aggregate(T3 * n3, gpu.timed(g3.replay, n3, args.warmup), gpu.world)
+        sec = t3["seconds"] / n3
+        if name == "decode":
+            uniq = len(set(idx3.flatten().tolist()))
+            nbytes = ROUTER_BYTES + uniq * EXPERT_BYTES3 + 2 * T3 * H * 4
+            ach = nbytes / sec / 1e9
+            roof = dict(bound="hbm", achieved=ach, peak=pk["hbm"], unit="GB/s", frac=ach / pk["hbm"], traffic=None,
+                        kernel="whole layer call (router + expert kernels)", bytes_per_launch=nbytes,
+                        distinct_experts=uniq, peak_source=f"{pk['source']} hbm_gbs (copy)")
+        else:
+            flop = 2.0 * T3 * K_TOP * 3 * H * I
+            ach = flop / sec / 1e12
+            roof = dict(bound="tensor", achieved=ach, peak=pk["bf16"], unit="TFLOP/s", frac=ach / pk["bf16"],
+                        traffic=None, kernel="whole layer call (router, permutation, both GEMMs)",
+                        flop_per_launch=flop, peak_source=f"{pk['source']} bf16_tflops (burst)")
+        res[name] = dict(T=T3, value=t3["value"], unit="tokens/s", ms_per_call=1e3 * sec, roofline=roof)
+        del ws3, x3, y3, g3
+    return dict(workload="3-bit block-32 weights, one 2048/512/512 top-10 layer, uniform routing",
+                dtype="3-bit x int8 block dots (decode); fp16 tensor-core products of exact hi/lo operands (prefill)",
+                **res)
+
+
+def mode_sweep(gpu, layers, Ws, args):
+    """Whole-layer time per call in GEMV and in grouped-GEMM mode for small T,
+    each replay running all resident layers so the experts come from HBM."""
+    torch, moeq = gpu.torch, gpu.moeq
+    import synth
+
+    nl = len(layers)
+    rows = []
+    for Ts in SWEEP_T:
+        wss = moeq.workspace(Ts, H, I, E, K_TOP, device=gpu.dev)
+        xsw = synth.make_x(Ts, H, seed=61 + Ts, device=gpu.dev)
+        ysw = torch.empty(Ts, H, device=gpu.dev)
+        row = dict(T=Ts)
+        for mname, mode in (("gemv", moeq.MODE_GEMV), ("gemm", moeq.MODE_GEMM)):
+            def stack(mode=mode):
+                for l in range(nl):
+                    moeq.layer_forward(xsw, Ws[l], layers[l].Wr, None, K_TOP, wss, y=ysw, mode=mode)
+
+            gs = gpu.graph(stack)
+            nrep = 5
+            row[mname + "_us_per_layer"] = 1e6 * gpu.timed(gs.replay, nrep, args.warmup) / (nrep * nl)
+            del gs
+        row["faster"] = "gemv" if row["gemv_us_per_layer"] <= row["gemm_us_per_layer"] else "gemm"
+        rows.append(row)
+        del wss, xsw, ysw
+    return rows
+
+
 def run_ours(args):
     import torch
 
@@ -212,229 +491,48 @@ def run_ours(args):
 
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
 
     import __graft_entry__
 
     __graft_entry__.build()
-    import quantized_mixture_experts_token_b300 as moeq
     import synth
 
-    pk = peaks()
+    gpu = Gpu(world, local)
+    moeq = gpu.moeq
     shape = synth.FULL
     nl = args.layers
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-
-            dist.barrier()
-
     # ---- resident weights: nl decode layers + one skewed prefill layer
-    layers = [synth.make_layer(shape, seed=0, layer=l, device=dev) for l in range(nl)]
+    layers = [synth.make_layer(shape, seed=0, layer=l, device=gpu.dev) for l in range(nl)]
     Ws = [moeq.ExpertWeights.from_layer(l) for l in layers]
-    pre_layer = synth.make_layer(shape, seed=0, layer=1000, device=dev, skew=True)
+    pre_layer = synth.make_layer(shape, seed=0, layer=1000, device=gpu.dev, skew=True)
     preW = moeq.ExpertWeights.from_layer(pre_layer)
     torch.cuda.synchronize()
 
-    # ---- decode: one token through the stack, residual chain x_{l+1} = x_l + moe_l(x_l)
+    # ---- headline: B=1 decode through the stack
+    dec = decode_stack(gpu, layers, Ws, DECODE_T, args.steps, args.warmup, seed=11 + rank, clocks=True)
     T = DECODE_T
-    ws = moeq.workspace(T, H, I, E, K_TOP, device=dev)
-    xs = [torch.empty(T, H, device=dev) for _ in range(nl + 1)]
-    xs[0].copy_(synth.make_x(T, H, seed=11 + rank, device=dev))
-
-    def decode_pass():
-        for l in range(nl):
-            moeq.layer_forward(xs[l], Ws[l], layers[l].Wr, None, K_TOP, ws, residual=True, y=xs[l + 1])
-
-    decode_pass()
-    torch.cuda.synchronize()
-    g_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dec):
-        decode_pass()
-    # a second graph whose expert-kernel launches are bracketed by events
-    ev_dec = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
-    moeq.trace_events(ev_dec)
-    g_dec_tr = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dec_tr):
-        decode_pass()
-    moeq.trace_events(None)
-
-    def timed(fn, steps, warmup):
-        for _ in range(warmup):
-            fn()
-        torch.cuda.synchronize()
-        barrier()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
-        for _ in range(steps):
-            fn()
-        e.record()
-        torch.cuda.synchronize()
-        barrier()
-        return s.elapsed_time(e) / 1e3
-
-    with ClockSampler(local) as clk:
-        t_dec = timed(g_dec.replay, args.steps, args.warmup)
-    clocks = clk.summary()
-    dec = aggregate(T * nl * args.steps, t_dec, world)
-
-    # expert-kernel time per launch (traced graph, replayed after warm-up)
-    for _ in range(3):
-        g_dec_tr.replay()
-    torch.cuda.synchronize()
-    k_ms = [ev_dec[2 * l].elapsed_time(ev_dec[2 * l + 1]) for l in range(nl)]
-    gemv_s = statistics.mean(k_ms) / 1e3
-    # algorithmic bytes of one decode expert launch: the selected experts' weights once
-    uniq = []
-    for l in range(nl):
-        _, idx, _ = moeq.layer_forward(xs[l], Ws[l], layers[l].Wr, None, K_TOP, ws, residual=True,
-                                       y=torch.empty_like(xs[l]), want_routing=True)
-        uniq.append(len(set(idx.flatten().tolist())))
-    dec_bytes = statistics.mean(uniq) * EXPERT_BYTES + 2 * T * H * 4
-    achieved = dec_bytes / gemv_s / 1e9
-    roof_dec = dict(bound="hbm", achieved=achieved, peak=pk["hbm"], unit="GB/s", frac=achieved / pk["hbm"],
-                    traffic=GEMV_TRAFFIC_BYTES, kernel="ffn_gemv_kernel<2>", bytes_per_launch=dec_bytes,
-                    launch_us=gemv_s * 1e6, peak_source=f"{pk['source']} hbm_gbs (copy)")
-
-    # decode end to end: pinned host token in, result out, every step
     x_host = torch.empty(T, H, pin_memory=True)
-    x_host.copy_(xs[0].cpu())
+    x_host.copy_(dec["xs"][0].cpu())
     y_host = torch.empty(T, H, pin_memory=True)
 
-    def e2e_step():
-        xs[0].copy_(x_host, non_blocking=True)
-        g_dec.replay()
-        y_host.copy_(xs[nl], non_blocking=True)
+    def e2e_step():  # pinned host token in, result out, every step
+        dec["xs"][0].copy_(x_host, non_blocking=True)
+        dec["graph"].replay()
+        y_host.copy_(dec["xs"][nl], non_blocking=True)
 
-    t_e2e = timed(e2e_step, args.steps, args.warmup)
-    dec_e2e = aggregate(T * nl * args.steps, t_e2e, world)
+    dec_e2e = aggregate(T * nl * args.steps, gpu.timed(e2e_step, args.steps, args.warmup), world)
 
-    # ---- prefill: a 4,096-token chunk through the skewed layer
-    out = {}
-    if not args.no_prefill:
-        Tp = PREFILL_T
-        wsp = moeq.workspace(Tp, H, I, E, K_TOP, device=dev)
-        xp = synth.make_x(Tp, H, seed=21 + rank, device=dev)
-        yp = torch.empty(Tp, H, device=dev)
+    # ---- 8 tokens per decode call through the stack
+    d8 = decode_stack(gpu, layers, Ws, DECODE_T8, args.steps, args.warmup, seed=13 + rank)
+    decode_t8 = dict(T=DECODE_T8, value=d8["agg"]["value"], unit="layer-tokens/s",
+                     us_per_layer=d8["layer_us"], roofline=d8["roof"])
+    del d8
 
-        def prefill_call():
-            moeq.layer_forward(xp, preW, pre_layer.Wr, pre_layer.bias, K_TOP, wsp, y=yp)
-
-        prefill_call()
-        torch.cuda.synchronize()
-        g_pre = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_pre):
-            prefill_call()
-        ev_pre = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        moeq.trace_events(ev_pre)
-        g_pre_tr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_pre_tr):
-            prefill_call()
-        moeq.trace_events(None)
-        psteps = max(3, args.steps // 2)
-        t_pre = timed(g_pre.replay, psteps, args.warmup)
-        pre = aggregate(Tp * psteps, t_pre, world)
-        for _ in range(3):
-            g_pre_tr.replay()
-        torch.cuda.synchronize()
-        gu_s = ev_pre[0].elapsed_time(ev_pre[1]) / 1e3
-        dn_s = ev_pre[2].elapsed_time(ev_pre[3]) / 1e3
-        P = Tp * K_TOP
-        gu_flop = 2.0 * P * 2 * I * H
-        dn_flop = 2.0 * P * H * I
-        ach = gu_flop / gu_s / 1e12
-        xp_host = torch.empty(Tp, H, pin_memory=True)
-        xp_host.copy_(xp.cpu())
-        yp_host = torch.empty(Tp, H, pin_memory=True)
-
-        def pre_e2e():
-            xp.copy_(xp_host, non_blocking=True)
-            g_pre.replay()
-            yp_host.copy_(yp, non_blocking=True)
-
-        t_pe = timed(pre_e2e, psteps, args.warmup)
-        pre_e2e_v = aggregate(Tp * psteps, t_pe, world)
-        out = dict(
-            value=pre["value"], unit="tokens/s", ms_per_chunk=1e3 * pre["seconds"] / psteps,
-            workload="prefill: 4,096-token chunk through one 2048/512/512 top-10 2-bit layer, Zipf(1.1)-skewed router",
-            dtype="fp16 tensor-core products of the exact 2-bit levels and an fp16 hi/lo split of the int8 activations, fp32 accumulate",
-            roofline=dict(bound="tensor", achieved=ach, peak=pk["bf16"], unit="TFLOP/s", frac=ach / pk["bf16"],
-                          traffic=GEMM_GU_TRAFFIC_BYTES, kernel="ffn_gemm_kernel<gate/up>", flop_per_launch=gu_flop,
-                          launch_us=gu_s * 1e6, peak_source=f"{pk['source']} bf16_tflops (burst; fp16 = bf16 rate)",
-                          down=dict(achieved=dn_flop / dn_s / 1e12, launch_us=dn_s * 1e6, flop_per_launch=dn_flop)),
-            e2e=dict(value=pre_e2e_v["value"], unit="tokens/s", h2d_bytes_per_step=Tp * H * 4,
-                     d2h_bytes_per_step=Tp * H * 4),
-            gpu_launches_per_chunk=PREFILL_LAUNCHES)
-
-    # ---- 3-bit weights: a 64-token verify window (decode path) and a 16,384-token
-    # prefill chunk, one layer with uniform routing (no bias)
-    bits3 = None
-    if not args.no_3bit:
-        l3 = synth.make_layer(synth.FULL3, seed=0, layer=2000, device=dev)
-        W3 = moeq.ExpertWeights.from_layer(l3)
-        torch.cuda.synchronize()
-        res3 = {}
-        for name, T3 in (("decode", VERIFY_T), ("prefill", PREFILL3_T)):
-            ws3 = moeq.workspace(T3, H, I, E, K_TOP, bits=3, device=dev)
-            x3 = synth.make_x(T3, H, seed=31 + rank, device=dev)
-            y3 = torch.empty(T3, H, device=dev)
-            _, idx3, _ = moeq.layer_forward(x3, W3, l3.Wr, None, K_TOP, ws3, y=y3, want_routing=True)
-            torch.cuda.synchronize()
-            g3 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g3):
-                moeq.layer_forward(x3, W3, l3.Wr, None, K_TOP, ws3, y=y3)
-            n3 = max(3, args.steps // 2)
-            t3 = aggregate(T3 * n3, timed(g3.replay, n3, args.warmup), world)
-            sec = t3["seconds"] / n3
-            if name == "decode":
-                uniq = len(set(idx3.flatten().tolist()))
-                nbytes = E * H * 4 + uniq * EXPERT_BYTES3 + 2 * T3 * H * 4
-                ach = nbytes / sec / 1e9
-                roof = dict(bound="hbm", achieved=ach, peak=pk["hbm"], unit="GB/s", frac=ach / pk["hbm"],
-                            traffic=None, kernel="whole layer call (router + expert kernels)",
-                            bytes_per_launch=nbytes, distinct_experts=uniq,
-                            peak_source=f"{pk['source']} hbm_gbs (copy)")
-            else:
-                flop = 2.0 * T3 * K_TOP * 3 * H * I
-                ach = flop / sec / 1e12
-                roof = dict(bound="tensor", achieved=ach, peak=pk["bf16"], unit="TFLOP/s", frac=ach / pk["bf16"],
-                            traffic=None, kernel="whole layer call (router, permutation, both GEMMs)",
-                            flop_per_launch=flop, peak_source=f"{pk['source']} bf16_tflops (burst)")
-            res3[name] = dict(T=T3, value=t3["value"], unit="tokens/s", ms_per_call=1e3 * sec, roofline=roof)
-            del ws3, x3, y3, g3
-        bits3 = dict(workload="3-bit block-32 weights, one 2048/512/512 top-10 layer, uniform routing",
-                     dtype="3-bit x int8 block dots (decode); fp16 tensor-core products of exact hi/lo operands (prefill)",
-                     **res3)
-        del l3, W3
-
-    # ---- expert-path crossover: whole-layer time per call in GEMV and in grouped-GEMM
-    # mode for small T, each replay running all nl resident layers so the selected
-    # experts come from HBM, not L2
-    sweep = None
-    if not args.no_sweep:
-        sweep = []
-        for Ts in SWEEP_T:
-            wss = moeq.workspace(Ts, H, I, E, K_TOP, device=dev)
-            xsw = synth.make_x(Ts, H, seed=61 + Ts, device=dev)
-            ysw = torch.empty(Ts, H, device=dev)
-            row = dict(T=Ts)
-            for mname, mode in (("gemv", moeq.MODE_GEMV), ("gemm", moeq.MODE_GEMM)):
-                def stack(mode=mode):
-                    for l in range(nl):
-                        moeq.layer_forward(xsw, Ws[l], layers[l].Wr, None, K_TOP, wss, y=ysw, mode=mode)
-
-                stack()
-                torch.cuda.synchronize()
-                gs = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gs):
-                    stack()
-                nrep = 5
-                row[mname + "_us_per_layer"] = 1e6 * timed(gs.replay, nrep, args.warmup) / (nrep * nl)
-                del gs
-            row["faster"] = "gemv" if row["gemv_us_per_layer"] <= row["gemm_us_per_layer"] else "gemm"
-            sweep.append(row)
-            del wss, xsw, ysw
+    prefill = None if args.no_prefill else prefill_chunk(gpu, pre_layer, preW, args, rank)
+    stack = None if args.no_stack else stack_prompt(gpu, layers, Ws, args, rank)
+    bits3 = None if args.no_3bit else bits3_section(gpu, args, rank)
+    sweep = None if args.no_sweep else mode_sweep(gpu, layers, Ws, args)
 
     status = moeq.device_status()
     if status:
@@ -448,20 +546,20 @@ def run_ours(args):
         cpu = dict(value=r, unit="tokens/s", cores=threads, kind="oracle",
                    sample=f"{n_tok} independent B=1 decode tokens through one layer ({dt:.1f} s wall)")
 
-    launches_per_step = 2 * nl  # fused routing kernel + expert GEMV per layer
+    launches_per_step = 2 * nl  # router kernel + expert kernel per layer
     line = dict(
-        metric=METRIC, value=dec["value"], unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
-        ms_per_step=1e3 * dec["seconds"] / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
-        dtype="int8 x 2-bit integer block dots, fp32 scales", data="synthetic",
+        metric=METRIC, value=dec["agg"]["value"], unit="tokens/s", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=1e3 * dec["agg"]["seconds"] / args.steps, higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype="int8 x 2-bit integer block dots, fp32 scales", data="synthetic",
         config=dict(workload=(f"decode: B=1 token through {nl} resident MoE layers (H=2048, E=512, I=512, top-10, "
                               "2-bit block-32 weights, residual between layers); value = per-layer tokens/s"),
-                    T=DECODE_T, layers=nl, stack_tokens_per_s=dec["value"] / nl,
+                    T=DECODE_T, layers=nl, stack_tokens_per_s=dec["agg"]["value"] / nl,
                     l2="inputs larger than L2: every step reads the selected experts of 48 distinct layers",
                     parallelism=f"replicas x{world}"),
-        roofline=roof_dec, cpu_baseline=cpu,
+        roofline=dec["roof"], cpu_baseline=cpu,
         e2e=dict(value=dec_e2e["value"], unit="tokens/s", h2d_bytes_per_step=T * H * 4, d2h_bytes_per_step=T * H * 4),
-        gpu_launches=launches_per_step * args.steps, clocks=clocks, prefill=out or None, bits3=bits3,
-        mode_sweep=sweep)
+        gpu_launches=launches_per_step * args.steps, clocks=dec["clocks"], decode_t8=decode_t8, prefill=prefill,
+        stack=stack, bits3=bits3, mode_sweep=sweep)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -478,7 +576,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=N_LAYERS)
     ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--stack-reps", type=int, default=2)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-3bit", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")

@@ -264,8 +264,9 @@ const char *moe_last_error_string(void);
  * "Strata - the details", "Speed (measured)"; this is the device-time
  * counterpart).  events: an array of n cudaEvent_t handles (n even) that the
  * caller created, or NULL to switch tracing off.  While set, every launch of
- * an expert kernel (the GEMV, and each of the two tensor-core GEMMs) on the
- * calling thread is bracketed by cudaEventRecord(events[c]) and
+ * an expert kernel (the GEMV, and each of the two tensor-core GEMMs) and of the
+ * prompt-chunk router GEMM (T > 64) on the calling thread is bracketed by
+ * cudaEventRecord(events[c]) and
  * cudaEventRecord(events[c+1]) on the call's stream, c advancing by 2 modulo
  * n and starting at 0 after each moe_trace_events call.  Works inside CUDA
  * graph capture (the records become graph nodes).  Returns MOEQ_ERR_ARG for an

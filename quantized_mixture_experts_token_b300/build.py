@@ -19,19 +19,32 @@ FLAGS = [
 ]
 
 
+PEAKS_LIB = os.path.join(HERE, "libmoeq_peaks.so")
+
+
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                  if f.endswith((".cu", ".cuh")) and f != "peaks.cu")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    deps = sources() + [os.path.join(ROOT, "include", "moeq.h"), __file__]
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(d) for d in deps):
-        return LIB
-    cmd = [NVCC, *FLAGS, os.path.join(CSRC, "moeq.cu"), "-o", LIB + ".tmp"]
+def _build_one(src, lib, deps, force, verbose):
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(d) for d in deps):
+        return lib
+    cmd = [NVCC, *FLAGS, src, "-o", lib + ".tmp"]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)
-    os.replace(LIB + ".tmp", LIB)
+    os.replace(lib + ".tmp", lib)
+    return lib
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """libmoeq.so (the layer) and libmoeq_peaks.so (its int8 peak microbenchmark)."""
+    inc = os.path.join(ROOT, "include")
+    _build_one(os.path.join(CSRC, "moeq.cu"), LIB, sources() + [os.path.join(inc, "moeq.h"), __file__], force,
+               verbose)
+    peaks_src = os.path.join(CSRC, "peaks.cu")
+    _build_one(peaks_src, PEAKS_LIB, [peaks_src, os.path.join(inc, "moeq_peaks.h"), __file__], force, verbose)
     return LIB
 
 

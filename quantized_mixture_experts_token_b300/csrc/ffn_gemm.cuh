@@ -94,6 +94,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// Bulk reduction of `bytes` of fp32 values from shared memory into global
+// memory (dst[i] += src[i]), tracked by this thread's bulk async-group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -133,10 +149,14 @@ template <bool GATEUP, int BITS>
 struct GemmCfg {
     static constexpr int NA = GATEUP ? 2 : 1;  // weight matrices per work item (gate + up, or down)
     static constexpr int BPB = 4 * BITS;
-    // operand ring, K = 64 per stage.  Two slots: with three or more in flight the
-    // gate/up outputs of some tiles came out wrong intermittently (cause not
-    // found); two slots gave identical results over repeated 4096-token runs.
+    // operand ring, K = 64 per stage (MOEQ_GEMM_STAGES overrides the depth at build time)
+#if defined(MOEQ_GEMM_STAGES_GU) && defined(MOEQ_GEMM_STAGES_DN)
+    static constexpr int STAGES = GATEUP ? MOEQ_GEMM_STAGES_GU : MOEQ_GEMM_STAGES_DN;
+#elif defined(MOEQ_GEMM_STAGES)
+    static constexpr int STAGES = MOEQ_GEMM_STAGES;
+#else
     static constexpr int STAGES = 2;
+#endif
     static constexpr int RSTAGES = (GATEUP && BITS == 3) ? 4 : 6;  // raw-code ring (runs further ahead)
     static constexpr int A_BYTES = kGmM * kGmK * 2;                // fp16 weight tile
     static constexpr int NAT = BITS == 3 ? 2 : 1;                  // weight tiles per matrix: hi (, lo)
@@ -149,11 +169,53 @@ struct GemmCfg {
     static constexpr int TMEM_COLS = 2 * ACC_COLS;  // double buffered: 512 (gate/up) or 256 (down)
     static constexpr int NUM_BARS = 2 * RSTAGES + 3 * STAGES + 5;
     static constexpr int MISC_BYTES = 8 * NUM_BARS + 16 + 3 * 2 * kGmN * 4;
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES;
+    // down: per epilogue warp two staging buffers of 16 tokens x its 32 rows of
+    // w * D (fp32) that it adds into y with bulk reductions
+    static constexpr int STAGE_BYTES = GATEUP ? 0 : 2 * 16 * kGmM * 4;
+    static constexpr size_t SMEM =
+        1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES + 128 + STAGE_BYTES;
     static constexpr int THREADS = 320;  // 10 warps, see the kernel
 };
 
+// Tracing builds: cycles each role spends in each wait, per CTA and kernel.
+#ifdef MOEQ_TIMELINE
+__device__ unsigned long long g_gemm_waits[2][256][16];
+#define MOEQ_GW(slot, expr)                                                  \
+    ([&]() {                                                                 \
+        const long long c0_ = clock64();                                     \
+        const bool r_ = (expr);                                              \
+        gw[slot] += (unsigned long long)(clock64() - c0_);                   \
+        return r_;                                                           \
+    }())
+#define MOEQ_GW_DECL unsigned long long gw[16] = {}; const long long gw_t0 = clock64()
+#define MOEQ_GW_FLUSH(lo, hi, total_slot)                                                      \
+    do {                                                                                       \
+        gw[total_slot] = (unsigned long long)(clock64() - gw_t0);                              \
+        for (int i_ = (lo); i_ <= (hi); ++i_)                                                  \
+            atomicAdd(&g_gemm_waits[GATEUP ? 0 : 1][blockIdx.x & 255][i_], gw[i_]);            \
+    } while (0)
+#else
+#define MOEQ_GW(slot, expr) (expr)
+#define MOEQ_GW_DECL \
+    do {             \
+    } while (0)
+#define MOEQ_GW_FLUSH(lo, hi, total_slot) \
+    do {                                  \
+    } while (0)
+#endif
+
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Named barrier over n threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %3, 0;\n\tbar.red.or.pred p, %1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(n), "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
 
 // Persistent grouped GEMM: one CTA per SM walks the work items q = blockIdx.x,
 // blockIdx.x + gridDim.x, ... where q = (tile, 128-row M block).  Each item is
@@ -193,8 +255,11 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     int *s_tok = reinterpret_cast<int *>(tmem_slot + 4);  // [2][kGmN] per accumulator buffer
     int *s_exp = s_tok + 2 * kGmN;
     float *s_wt = reinterpret_cast<float *>(s_exp + 2 * kGmN);
+    float *s_stage = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_wt + 2 * kGmN) + 127) & ~(uintptr_t)127);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint64_t wl = wait_limit();
+    constexpr int TLK = GATEUP ? 5 : 6;  // timeline kernel id (tracing builds)
     if (tid == 0) {
         for (int i = 0; i < R; ++i) {
             mbar_init(smem_u32(&raw_full[i]), 1);
@@ -230,6 +295,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
+        MOEQ_GW_DECL;
         const uint64_t pol = l2_evict_first();
         // raw cursor: runs up to R stages ahead of the operand cursor
         int rj = 0, rks = 0, rs = 0, graw = 0;
@@ -245,7 +311,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             for (int ks = 0; ks < nk; ++ks) {
                 const int g = j * nk + ks;
                 for (; graw < G && graw < g + R; ++graw) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&raw_empty[rs]), rph ^ 1, abort_flag))) {
+                    if (!__all_sync(0xffffffffu, MOEQ_GW(0, mbar_wait(smem_u32(&raw_empty[rs]), rph ^ 1, abort_flag, wl)))) {
                         ok = false;
                         break;
                     }
@@ -278,7 +344,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 if (!ok) break;
                 // B rows of this stage: hi/lo of sorted pairs p0 .. p0 + nround, K columns
                 // [64 ks, 64 ks + 64), one contiguous run of 128-byte rows per half
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag))) {
+                if (!__all_sync(0xffffffffu, MOEQ_GW(1, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag, wl)))) {
                     ok = false;
                     break;
                 }
@@ -298,6 +364,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 }
             }
         }
+        if (lane == 0) MOEQ_GW_FLUSH(0, 2, 2);
         if (!ok && lane == 0) {  // drain the copies still in flight
             for (int g2 = max(0, graw - R); g2 < graw; ++g2)
                 mbar_drain(smem_u32(&raw_full[g2 % R]), (g2 / R) & 1, abort_flag);
@@ -307,6 +374,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
+            MOEQ_GW_DECL;
             // descriptors: slot s, matrix m, K step kk = base + ((s*SLOT + m*A) >> 4) + 2 kk
             const uint64_t d0 = sw128_desc(smem_u32(slots));
             int s = 0;
@@ -318,15 +386,18 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 if (j + 1 < nq) next = item_tile(j + 1);  // consumed one item later
                 const uint32_t idesc = f16_idesc(kGmM, (tl.n + 15) & ~15);
                 const int buf = j & 1;
-                if (!mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag)) break;
+                if (!MOEQ_GW(3, mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag, wl))) break;
+                MOEQ_TL_TAG(TLK, 0, ((unsigned)j << 8) | blockIdx.x);
                 tc_fence_after();
                 const uint32_t acc0 = tmem + (uint32_t)(buf * C::ACC_COLS);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!mbar_wait(smem_u32(&a_full[s]), ph, abort_flag) || !mbar_wait(smem_u32(&b_full[s]), ph, abort_flag)) {
+                    if (!MOEQ_GW(4, mbar_wait(smem_u32(&a_full[s]), ph, abort_flag, wl)) ||
+                        !MOEQ_GW(5, mbar_wait(smem_u32(&b_full[s]), ph, abort_flag, wl))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    if (ks == 0) MOEQ_TL_TAG(TLK, 1, ((unsigned)j << 8) | blockIdx.x);
                     const uint64_t ds = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
                     const uint64_t dbh = ds + (uint64_t)((C::NAT * NA * C::A_BYTES) >> 4);
                     const uint64_t dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
@@ -349,7 +420,9 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     }
                 }
                 if (ok) mma_commit(smem_u32(&acc_full[buf]));
+                MOEQ_TL_TAG(TLK, 2, ((unsigned)j << 8) | blockIdx.x);
             }
+            MOEQ_GW_FLUSH(3, 6, 6);
             // every MMA issued above is complete once this commit lands
             mma_commit(smem_u32(drain));
             mbar_drain(smem_u32(drain), 0, abort_flag);
@@ -358,11 +431,13 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
     } else if (warp < 6) {
         // ----------------------------------------------------------- unpack
         const int r = tid - 64;  // weight row of the tile
+        MOEQ_GW_DECL;
         int rs = 0, s = 0;
         uint32_t rph = 0, ph = 0;
         bool ok = true;
         for (int g = 0; g < G && ok; ++g) {
-            if (!mbar_wait(smem_u32(&raw_full[rs]), rph, abort_flag)) break;
+            if (!MOEQ_GW(7, mbar_wait(smem_u32(&raw_full[rs]), rph, abort_flag, wl))) break;
+            if (r == 0 && g % nk == 0) MOEQ_TL_TAG(TLK, 5, ((unsigned)(g / nk) << 8) | blockIdx.x);
             const unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
             uint32_t cw[NA][2][BITS];
             uint16_t sbits[NA][2];
@@ -380,7 +455,7 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 rs = 0;
                 rph ^= 1;
             }
-            if (!mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag)) break;
+            if (!MOEQ_GW(8, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag, wl))) break;
             unsigned char *sb = slots + (size_t)s * C::SLOT_BYTES;
 #pragma unroll
             for (int m = 0; m < NA; ++m) {
@@ -435,17 +510,21 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             }
             fence_proxy_async();
             mbar_arrive(smem_u32(&a_full[s]));
+            if (r == 0 && g % nk == nk - 1) MOEQ_TL_TAG(TLK, 6, ((unsigned)(g / nk) << 8) | blockIdx.x);
             if (++s == S) {
                 s = 0;
                 ph ^= 1;
             }
         }
+        if (r == 0) MOEQ_GW_FLUSH(7, 9, 9);
     } else {
         // --------------------------------------------------------- epilogue
         const int et = tid - 192;                 // 0..127: table entry this thread loads
         const int row = 32 * (warp & 3) + lane;   // accumulator lane = weight row
         const uint32_t tl_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        MOEQ_GW_DECL;
         bool dead = false;  // after an abort the loop still meets every named barrier
+        int nstage = 0;     // staging buffers used so far (down)
         for (int j = 0; j < nq; ++j) {
             const Tile tl = item_tile(j);
             const int m0 = item_m0(j);
@@ -467,11 +546,13 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             }
             named_sync(1, 128);
             if (dead) continue;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acc_full[buf]), (j >> 1) & 1, abort_flag))) {
+            // one decision for all four epilogue warps (they meet at named barriers below)
+            if (named_sync_or(3, 128, !MOEQ_GW(10, mbar_wait(smem_u32(&acc_full[buf]), (j >> 1) & 1, abort_flag, wl)))) {
                 dead = true;
                 continue;
             }
             tc_fence_after();
+            if (et == 0) MOEQ_TL_TAG(TLK, 3, ((unsigned)j << 8) | blockIdx.x);
             const int *etab = s_exp + buf * kGmN;
             const uint32_t acc = tl_lane + (uint32_t)(buf * C::ACC_COLS);
             for (int c0 = 0; c0 < nround; c0 += 16) {
@@ -496,19 +577,45 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                 } else {
                     const int *ttab = s_tok + buf * kGmN;
                     const float *wtab = s_wt + buf * kGmN;
+                    if (a.y) {
+                        // w * D of these 16 pairs -> this warp's staging buffer [pair][its 32
+                        // rows] -> one 128-byte bulk reduction per pair into
+                        // y[token][m0 + 32 (warp % 4) ...]; warps proceed independently
+                        const int q = warp & 3;
+                        float *stg = s_stage + ((nstage & 1) * 4 + q) * 16 * 32;
+                        bulk_wait_read<1>();  // (issuing lanes) this buffer's previous reductions have read it
+                        __syncwarp();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int jc = c0 + jj;
-                        if (jc >= nval) break;
-                        const float D = acc0[jj] * exp2i(etab[jc]);
-                        if (a.y) atomicAdd(a.y + (size_t)ttab[jc] * a.H + m0 + row, wtab[jc] * D);
-                        if (a.out_sorted) a.out_sorted[(size_t)(p0 + jc) * a.H + m0 + row] = D;
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int jc = c0 + jj;
+                            stg[jj * 32 + lane] = wtab[jc] * acc0[jj] * exp2i(etab[jc]);
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane < 16) {
+                            if (c0 + lane < nval)
+                                bulk_reduce_add_f32(a.y + (size_t)ttab[c0 + lane] * a.H + m0 + 32 * q,
+                                                    smem_u32(stg + lane * 32), 32 * 4);
+                            bulk_commit();
+                        }
+                        ++nstage;
+                    }
+                    if (a.out_sorted) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int jc = c0 + jj;
+                            if (jc >= nval) break;
+                            a.out_sorted[(size_t)(p0 + jc) * a.H + m0 + row] = acc0[jj] * exp2i(etab[jc]);
+                        }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[buf]));
+            if (et == 0) MOEQ_TL_TAG(TLK, 4, ((unsigned)j << 8) | blockIdx.x);
         }
+        if (!GATEUP && lane < 16) bulk_wait_all();  // reductions done before the CTA exits
+        if (et == 0) MOEQ_GW_FLUSH(10, 11, 11);
     }
     tc_fence_before();
     __syncthreads();

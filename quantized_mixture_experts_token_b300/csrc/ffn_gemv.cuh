@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
     const int nIB = a.I / 32, KBH = a.H / 32;
     const int u = blockIdx.x / nIB, ib = blockIdx.x % nIB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t wl = wait_limit();
 
     extern __shared__ __align__(128) unsigned char smem[];
     const GemvSmem L = gemv_smem(a.H, BITS, a.kc, a.rc, a.tc);
@@ -314,8 +315,10 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
     if (warp == 0 && lane < 4) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tm[lane])) : "memory");
     __syncthreads();
 
+    MOEQ_TL(2, 0);
     pdl_wait();  // the router logits (or routing records) and quantised x of this call are complete
     pdl_trigger();
+    MOEQ_TL(2, 1);
     // quantised activation rows (codes already in the block dot's order, block
     // scales, block code sums) of the given tokens into staging rows 0, 1, ...
     // of shared memory, one bulk copy each (thread 0)
@@ -337,6 +340,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
     }
     int e = 0, pb = 0, ne = 0;
     const bool have = gemv_unit<PER>(a, u, tok, wt, e, pb, ne);  // uniform over the CTA
+    MOEQ_TL(2, 2);
     const bool bad = have && (e < 0 || e >= a.E);
     if (!have || bad || ne <= 0) {
         if (bad && tid == 0) set_status(MOEQ_STATUS_BAD_INDEX);
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
             xrow[tid] = tok[tid];
         }
         if (!x_ready) {
-            const bool ok = mbar_wait(bar_x, x_ph & 1, abort_flag);
+            const bool ok = mbar_wait(bar_x, x_ph & 1, abort_flag, wl);
             if (__syncthreads_or(!ok)) {
                 failed = true;
                 break;
@@ -414,6 +418,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
             ++x_ph;
             x_pending = false;
             x_ready = x_staged;
+            MOEQ_TL(2, 3);
         } else {
             __syncthreads();
         }
@@ -430,13 +435,14 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
                 gu_ready = false;
             }
             if (!gu_ready) {
-                const bool ok = mbar_wait(bar_gu, gu_ph & 1, abort_flag);
+                const bool ok = mbar_wait(bar_gu, gu_ph & 1, abort_flag, wl);
                 if (__syncthreads_or(!ok)) {
                     failed = true;
                     break;
                 }
                 ++gu_ph;
                 gu_ready = true;
+                MOEQ_TL(2, 4);
             }
             const int kb0 = gc * a.kc, nkb = min(a.kc, KBH - kb0);
 #define MOEQ_GU(NT_)                                                                                             \
@@ -458,6 +464,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
 #pragma unroll
         for (int s = 0; s < kGvTok; ++s) part[((m * 4 + q4) * kGvTok + s) * 32 + lane] = acc[s];
         __syncthreads();
+        MOEQ_TL(2, 5);
         // 3. SwiGLU and re-quantisation of this I-block, one warp per token
         if (warp < nt) {
             const int s = warp;
@@ -481,6 +488,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
             if (a.sh_out && lane == 0) a.sh_out[p * nIB + ib] = sh;
         }
         __syncthreads();
+        MOEQ_TL(2, 6);
         // 4. down projection of I-block ib, 4 consecutive output rows per thread
         for (int dc = 0; dc < ndc; ++dc) {
             if (d_chunk != dc) {
@@ -490,13 +498,14 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
                 d_ready = false;
             }
             if (!d_ready) {
-                const bool ok = mbar_wait(bar_d, d_ph & 1, abort_flag);
+                const bool ok = mbar_wait(bar_d, d_ph & 1, abort_flag, wl);
                 if (__syncthreads_or(!ok)) {
                     failed = true;
                     break;
                 }
                 ++d_ph;
                 d_ready = true;
+                MOEQ_TL(2, 7);
             }
             const int r0 = dc * a.rc, nr = min(a.rc, a.H - r0);
             for (int g = tid; g < nr / 4; g += blockDim.x) {
@@ -526,6 +535,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
         }
         __syncthreads();
     }
+    MOEQ_TL(2, 8);
     if (failed && tid == 0) {
         // drain the copies still in flight before the CTA's shared memory is released
         if (!gu_ready) mbar_drain(bar_gu, gu_ph & 1, abort_flag);

@@ -17,6 +17,7 @@
 #include "permute.cuh"
 #include "quant.cuh"
 #include "route.cuh"
+#include "route_tc.cuh"
 
 using namespace moeq;
 
@@ -248,6 +249,34 @@ int route_gemv_dispatch(const float *x, int T, int H, const float *Wr, const flo
     return launch_route_gemv<32>(x, T, H, Wr, bias, E, logits, tail, s);
 }
 
+int tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint64_t esize, uint64_t cols, uint64_t rows,
+            uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle swz);
+int max_smem_optin();
+
+// Router logits of a prompt chunk on the tensor cores (3xTF32).
+int route_tc(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits, cudaStream_t s) {
+    RouteTcArgs g{};
+    g.T = T;
+    g.H = H;
+    g.E = E;
+    g.bias = bias;
+    g.logits = logits;
+    if (int rc = tmap_2d(&g.tm_x, x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)H, (uint64_t)T, kRtK, kRtM,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+        return rc;
+    if (int rc = tmap_2d(&g.tm_w, Wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)H, (uint64_t)E, kRtK, kRtN,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+        return rc;
+    if ((int)kRtSmem > max_smem_optin()) return fail(MOEQ_ERR_SHAPE, "router GEMM needs %zu bytes of shared memory", kRtSmem);
+    cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "router smem attribute: %s", cudaGetErrorString(e));
+    dim3 grid((E + kRtN - 1) / kRtN, (T + kRtM - 1) / kRtM);
+    trace_begin(s);
+    route_tc_kernel<<<grid, 320, kRtSmem, s>>>(g);
+    trace_end(s);
+    return cuda_check("route_tc_kernel");
+}
+
 // Router logits + top-k (unfused).
 int route_unfused(const float *x, int T, int H, const float *Wr, const float *bias, int E, int k, int32_t *idx,
                   float *w, float *logits, cudaStream_t s) {
@@ -255,8 +284,7 @@ int route_unfused(const float *x, int T, int H, const float *Wr, const float *bi
         DecodeTail none{};
         if (int rc = route_gemv_dispatch(x, T, H, Wr, bias, E, logits, none, s)) return rc;
     } else {
-        dim3 grid((E + kSgBN - 1) / kSgBN, (T + kSgBM - 1) / kSgBM);
-        route_sgemm_kernel<<<grid, 256, 0, s>>>(x, T, H, Wr, bias, E, logits);
+        if (int rc = route_tc(x, T, H, Wr, bias, E, logits, s)) return rc;
     }
     topk_dispatch(logits, T, E, k, idx, w, s);
     return MOEQ_OK;
@@ -280,7 +308,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 // 2-D TMA map over a row-major [rows][cols] array of esize-byte elements with
 // box {box_c, box_r}; zero fill outside the array.
 int tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint64_t esize, uint64_t cols, uint64_t rows,
-            uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+            uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle swz) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (!enc) return fail(MOEQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     cuuint64_t dims[2] = {cols, rows};
@@ -309,10 +337,10 @@ int launch_gemv(GemvArgs g, int T, int k, int E, cudaStream_t s) {
     const uint64_t rows = (uint64_t)E * (uint64_t)(g.H / 32);  // (expert, K-block) rows of gate/up
     for (int m = 0; m < 2; ++m) {
         if (int rc = tmap_2d(&g.tm[m], g.codes[m], CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)g.I * BITS, rows,
-                             32 * BITS, (uint32_t)g.kc))
+                             32 * BITS, (uint32_t)g.kc, CU_TENSOR_MAP_SWIZZLE_NONE))
             return rc;
         if (int rc = tmap_2d(&g.tm[2 + m], g.scales[m], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)g.I, rows, 32,
-                             (uint32_t)g.kc))
+                             (uint32_t)g.kc, CU_TENSOR_MAP_SWIZZLE_NONE))
             return rc;
     }
     cudaError_t e = cudaFuncSetAttribute(ffn_gemv_kernel<BITS, PER>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -779,6 +807,34 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
         return rc;
     return ok();
 }
+
+#ifdef MOEQ_TIMELINE
+// Tracing build only (not part of the C ABI): copies up to max_entries
+// timeline entries (2 x uint64 each) to host memory, returns their number and
+// clears the ring.
+int moe_timeline_read(unsigned long long *host, int max_entries) {
+    cudaDeviceSynchronize();
+    unsigned n = 0;
+    cudaMemcpyFromSymbol(&n, g_tl_n, sizeof n);
+    const int m = (int)std::min<unsigned>(std::min<unsigned>(n, kTlEntries), (unsigned)max_entries);
+    if (m > 0) cudaMemcpyFromSymbol(host, g_tl, (size_t)m * 16);
+    unsigned zero = 0;
+    cudaMemcpyToSymbol(g_tl_n, &zero, sizeof zero);
+    return m;
+}
+#endif
+
+#ifdef MOEQ_TIMELINE
+// Tracing build only: copies the per-CTA wait counters of the two GEMMs
+// ([2][256][16] uint64) to host memory and clears them.
+int moe_gemm_waits_read(unsigned long long *host) {
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(host, g_gemm_waits, sizeof(g_gemm_waits));
+    static unsigned long long zero[2][256][16];
+    cudaMemcpyToSymbol(g_gemm_waits, zero, sizeof(zero));
+    return 0;
+}
+#endif
 
 int moe_set_wait_limit(uint64_t ns) {
     constexpr uint64_t kMaxLimitNs = 60ull * 1000000000ull;

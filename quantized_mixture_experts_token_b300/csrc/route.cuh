@@ -60,7 +60,28 @@ __device__ __forceinline__ void warp_topk(const float *row, int E, int k, int32_
             ++c;
         }
     const int total = __reduce_add_sync(0xffffffffu, c);
-    if (total <= 64) {
+    if (total <= 32) {
+        // usual case: one candidate per lane, ranked by 32 register shuffles
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int pos = incl - c;
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if ((cm >> i) & 1u) s_cand[wid][pos++] = make_uint2(key[i], (uint32_t)(lane + 32 * i));
+        __syncwarp();
+        const uint2 me = lane < total ? s_cand[wid][lane] : make_uint2(0u, 0xffffffffu);
+        int r = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t ok = __shfl_sync(0xffffffffu, me.x, j), oe = __shfl_sync(0xffffffffu, me.y, j);
+            r += (j < total) && ((ok > me.x) || (ok == me.x && oe < me.y));
+        }
+        if (lane < total && r < k) s_top[wid][r] = me;
+    } else if (total <= 64) {
         int incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -234,6 +255,7 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
     extern __shared__ __align__(16) unsigned char rsm[];
     const RouteSmem L = route_smem(H, E);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t wl = wait_limit();
     const int e0 = blockIdx.x * kRouteRows;
     const int nr = min(kRouteRows, E - e0);
     const int hc = min(H, kRouteHC), nhc = (H + hc - 1) / hc;
@@ -258,30 +280,10 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
         }
     };
     if (tid == 0) issue(0);  // router weights are read-only inputs: no need to wait for the stream
+    MOEQ_TL(1, 0);
     pdl_trigger();
     pdl_wait();  // x (and the buffers written below) belong to earlier work on the stream
-
-    if (tail.mode > 0) {
-        // y = residual ? x : 0, before any expert adds into it
-        const size_t n = (size_t)T * H;
-        for (size_t i = (size_t)blockIdx.x * blockDim.x + tid; i < n; i += (size_t)gridDim.x * blockDim.x)
-            tail.y[i] = tail.residual ? x[i] : 0.0f;
-        // x quantised per 32-block for the expert kernel: warp j of CTA b takes
-        // blocks b + j*gridDim, b + (j+8)*gridDim, ... (one block per CTA first)
-        const int KBH = H / 32;
-        for (int job = blockIdx.x + warp * gridDim.x; job < T * KBH; job += gridDim.x * 8) {
-            const int t = job / KBH, b = job - t * KBH;
-            const float v = x[(size_t)t * H + 32 * b + lane];
-            const float sc = block_scale(warp_absmax(v));
-            const int q = block_code(v, sc);
-            tail.qx[(size_t)t * H + 32 * b + (tail.bits == 2 ? pack_pos2(lane) : lane)] = (int8_t)q;
-            const int qs = warp_sum_int(q);
-            if (lane == 0) {
-                tail.sx[job] = sc;
-                tail.xsum[job] = qs;
-            }
-        }
-    }
+    MOEQ_TL(1, 1);
 
     int loaded = 0;
     bool ready = false, failed = false;
@@ -301,13 +303,14 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
                 ready = false;
             }
             if (!ready) {
-                const bool ok = mbar_wait(bar, ph & 1, &s_abort);
+                const bool ok = mbar_wait(bar, ph & 1, &s_abort, wl);
                 if (__syncthreads_or(!ok)) {
                     failed = true;
                     break;
                 }
                 ++ph;
                 ready = true;
+                MOEQ_TL(1, 2);
             }
             const int c0 = c * hc, w = min(hc, H - c0);
             const int ws = w / 8;  // multiple of 16
@@ -337,7 +340,31 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
         }
         __syncthreads();
     }
+    // after the logits (the critical output): x is now in this SM's L1
+    if (tail.mode > 0) {
+        // y = residual ? x : 0, before any expert adds into it
+        const size_t n = (size_t)T * H;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + tid; i < n; i += (size_t)gridDim.x * blockDim.x)
+            tail.y[i] = tail.residual ? x[i] : 0.0f;
+        // x quantised per 32-block for the expert kernel: warp j of CTA b takes
+        // blocks b + j*gridDim, b + (j+8)*gridDim, ... (one block per CTA first)
+        const int KBH = H / 32;
+        for (int job = blockIdx.x + warp * gridDim.x; job < T * KBH; job += gridDim.x * 8) {
+            const int t = job / KBH, b = job - t * KBH;
+            const float v = x[(size_t)t * H + 32 * b + lane];
+            const float sc = block_scale(warp_absmax(v));
+            const int q = block_code(v, sc);
+            tail.qx[(size_t)t * H + 32 * b + (tail.bits == 2 ? pack_pos2(lane) : lane)] = (int8_t)q;
+            const int qs = warp_sum_int(q);
+            if (lane == 0) {
+                tail.sx[job] = sc;
+                tail.xsum[job] = qs;
+            }
+        }
+    }
+
     if (failed && tid == 0 && !ready) mbar_drain(bar, ph & 1, &s_abort);  // the copy in flight lands first
+    MOEQ_TL(1, 3);
     if (tail.mode < 2) return;
 
     // ---- the last CTA to finish ranks every token and groups the pairs by expert.
@@ -411,6 +438,7 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
         tail.ctrl[1] = s_nunits;
         tail.ctrl[0] = 0;  // re-arm the arrival counter for the next call
     }
+    MOEQ_TL(1, 4);
 }
 
 // ------------------------------------------------- router logits, large T

@@ -35,6 +35,23 @@ def test_library_exports_every_declared_symbol(L):
     assert L.moe_version().decode().startswith("moeq")
 
 
+def test_peaks_library_exports_its_header():
+    import ctypes as C
+
+    src = open(os.path.join(ROOT, "include", "moeq_peaks.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+    assert names == ["moe_peak_mma_s8"]
+    import __graft_entry__
+
+    __graft_entry__.build()
+    lib = C.CDLL(os.path.join(ROOT, "quantized_mixture_experts_token_b300", "libmoeq_peaks.so"))
+    for n in names:
+        assert hasattr(lib, n), n
+    lib.moe_peak_mma_s8.argtypes = [C.c_int, C.c_int, C.c_void_p]
+    assert lib.moe_peak_mma_s8(0, 1, None) == -1  # argument check, nothing launched
+
+
 def test_workspace_bytes_host_logic(L):
     n1 = moeq.workspace_bytes(1, 2048, 512, 512, 10)
     n8 = moeq.workspace_bytes(8, 2048, 512, 512, 10)

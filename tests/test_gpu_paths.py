@@ -124,7 +124,6 @@ def test_decode_stack_in_cuda_graph(stack, cuda_lib, T):
     xs = [torch.empty(T, shape.H, device=_dev()) for _ in range(nl + 1)]
     x0 = synth.make_x(T, shape.H, seed=700 + T)
     xs[0].copy_(x0)
-    idxs = [torch.empty(T, shape.k, dtype=torch.int32, device=_dev()) for _ in range(nl)]
 
     def run():
         for l in range(nl):
@@ -137,18 +136,26 @@ def test_decode_stack_in_cuda_graph(stack, cuda_lib, T):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         run()
-    outs = []
-    for _ in range(2):
+    skipped = 0
+    for rep in range(2):
         for t in xs[1:]:
             t.zero_()
         g.replay()
         torch.cuda.synchronize()
-        outs.append([t.cpu().numpy().copy() for t in xs])
-    assert all(np.array_equal(a, b) or np.abs(a - b).max() <= 1e-6 * np.abs(a).max()
-               for a, b in zip(outs[0], outs[1]))
-    xh = outs[0]
+        # (replays need not agree bit for bit: the experts add into y with fp32
+        # atomics, and the residual chain carries those roundings on; each
+        # replay is checked against the oracle on its own inputs)
+        skipped += _check_stack(cuda_lib, shape, layers, Ws, ws, [t.cpu().numpy().copy() for t in xs], T)
+    print(f"decode stack T={T}: {skipped} token-layers skipped for a routing margin below 1e-3")
+    assert skipped <= 2 * nl * T // 4
+    assert cuda_lib.device_status() == 0
+
+
+def _check_stack(cuda_lib, shape, layers, Ws, ws, xh, T):
+    from oracle.checks import compare_layer_output
+
     skipped = 0
-    for l in range(nl):
+    for l in range(len(layers)):
         lnp = layers[l].numpy()
         ref = oracle.layer(xh[l], lnp[0], None, lnp[2], lnp[3], shape.bits, shape.k, detail=True)
         _, idx_dev, _ = cuda_lib.layer_forward(torch.from_numpy(xh[l]).to(_dev()), Ws[l], layers[l].Wr, None, shape.k,
@@ -165,12 +172,8 @@ def test_decode_stack_in_cuda_graph(stack, cuda_lib, T):
         dy = xh[l + 1].astype(np.float64) - xh[l].astype(np.float64)
         sub = {key: v[keep] for key, v in ref.items()}
         rms = float(np.sqrt(np.mean(ref["y"].astype(np.float64) ** 2)))
-        from oracle.checks import compare_layer_output
-
         compare_layer_output(dy[keep], sub, lnp[2][2], lnp[3][2], shape.bits, rms=rms, delta=DELTA[1])
-    print(f"decode stack T={T}: {skipped} token-layers skipped for a routing margin below 1e-3")
-    assert skipped <= nl * T // 4
-    assert cuda_lib.device_status() == 0
+    return skipped
 
 
 # --------------------------------------------------- combine against the oracle
@@ -199,4 +202,21 @@ def test_combine_against_oracle(request, cuda_lib, case_name, T, residual):
         mag += np.abs(x.numpy().astype(np.float64))
     bound = (k + 3) * 2.0**-24 * mag + 1e-30
     assert (np.abs(yd - ref["y"].astype(np.float64)) <= bound + 2.0**-24 * np.abs(ref["y"])).all()
+    assert cuda_lib.device_status() == 0
+
+
+@pytest.mark.parametrize("H,T", [(384, 37), (256, 3)])
+def test_gemv_other_hidden_sizes(cuda_lib, H, T):
+    """The decode expert kernel at hidden sizes other than the model's (12 and 8
+    K-blocks), with more tokens than one pass holds (T = 37)."""
+    shape = synth.LayerShape(H=H, I=128, E=8, k=2)
+    case = LayerCase(shape, seed=31, device="cpu")
+    x = case.x(T, seed=900 + H)
+    ws = _ws(cuda_lib, T, shape)
+    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), case.W, case.dev.Wr, None, shape.k, ws, mode=1,
+                                       want_routing=True)
+    torch.cuda.synchronize()
+    ref = case.oracle(x)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    case.check_y(y.cpu().numpy(), ref, delta=DELTA[1])
     assert cuda_lib.device_status() == 0
