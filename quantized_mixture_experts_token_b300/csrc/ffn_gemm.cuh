@@ -174,7 +174,9 @@ struct GemmCfg {
     static constexpr int STAGE_BYTES = GATEUP ? 0 : 2 * 16 * kGmM * 4;
     static constexpr size_t SMEM =
         1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES + 128 + STAGE_BYTES;
-    static constexpr int THREADS = 320;  // 10 warps, see the kernel
+    static constexpr int UNPACK = 128;                   // unpack threads (warps 2 .. 2 + UNPACK/32 - 1)
+    static constexpr int THREADS = 64 + UNPACK + 128;    // producer, MMA, unpack, epilogue warps
+    static constexpr int PIECES = NA * 2 * 128 / UNPACK;  // (matrix, K-block) pieces per unpack thread and stage
 };
 
 // Tracing builds: cycles each role spends in each wait, per CTA and kernel.
@@ -231,7 +233,7 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag,
 // every role leaves its loop, copies and MMAs are drained and TMEM is freed.
 template <bool GATEUP, int BITS>
-__global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant__ GemmArgs a) {
+__global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_kernel(const __grid_constant__ GemmArgs a) {
     using C = GemmCfg<GATEUP, BITS>;
     constexpr int NA = C::NA, BPB = C::BPB, S = C::STAGES, R = C::RSTAGES;
     const int MT = (GATEUP ? a.I : a.H) / kGmM;
@@ -259,14 +261,14 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t wl = wait_limit();
-    constexpr int TLK = GATEUP ? 5 : 6;  // timeline kernel id (tracing builds)
+    [[maybe_unused]] constexpr int TLK = GATEUP ? 5 : 6;  // timeline kernel id (tracing builds)
     if (tid == 0) {
         for (int i = 0; i < R; ++i) {
             mbar_init(smem_u32(&raw_full[i]), 1);
-            mbar_init(smem_u32(&raw_empty[i]), 128);
+            mbar_init(smem_u32(&raw_empty[i]), C::UNPACK);
         }
         for (int i = 0; i < S; ++i) {
-            mbar_init(smem_u32(&a_full[i]), 128);
+            mbar_init(smem_u32(&a_full[i]), C::UNPACK);
             mbar_init(smem_u32(&b_full[i]), 1);
             mbar_init(smem_u32(&slot_empty[i]), 1);
         }
@@ -349,8 +351,10 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                     break;
                 }
                 const uint32_t bbar = smem_u32(&b_full[s]);
+                // tiles of <= kGmN/2 rows: the lo rows follow the hi rows, so that one MMA
+                // of N = 2 nround forms both products (see the MMA warp)
                 const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + C::NAT * NA * C::A_BYTES),
-                               blo = bhi + C::B_BYTES;
+                               blo = nround <= kGmN / 2 ? bhi + (uint32_t)(nround * 128) : bhi + C::B_BYTES;
                 if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(2 * nround * kGmK * 2));
                 __syncwarp();
                 if (lane < 2)
@@ -384,7 +388,14 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             for (int j = 0; j < nq && ok; ++j) {
                 const Tile tl = next;
                 if (j + 1 < nq) next = item_tile(j + 1);  // consumed one item later
-                const uint32_t idesc = f16_idesc(kGmM, (tl.n + 15) & ~15);
+                // a tile of nround <= kGmN / 2 rows has B = [hi rows; lo rows] and takes one MMA
+                // of N = 2 nround per product: hi into accumulator columns [0, nround), lo into
+                // [nround, 2 nround), added in the epilogue (an MMA costs about the same down
+                // to N = 64, so this halves the time of small tiles); larger tiles take two MMAs
+                // (hi, lo) into the same columns
+                const int nround = (tl.n + 15) & ~15;
+                const bool cat = nround <= kGmN / 2;
+                const uint32_t idesc = f16_idesc(kGmM, cat ? 2 * nround : nround);
                 const int buf = j & 1;
                 if (!MOEQ_GW(3, mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag, wl))) break;
                 MOEQ_TL_TAG(TLK, 0, ((unsigned)j << 8) | blockIdx.x);
@@ -408,8 +419,8 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
                             const uint64_t ad = ds + (uint64_t)((m * C::A_BYTES) >> 4) + 2 * kk;
                             const uint32_t acc = acc0 + (uint32_t)(m * kGmN);
                             mma_f16(acc, ad, dbh + 2 * kk, idesc, (ks | kk) != 0);
-                            mma_f16(acc, ad, dbl + 2 * kk, idesc, 1u);
-                            if (C::NAT == 2)  // 3-bit: the weight panel's lo part against B hi
+                            if (!cat) mma_f16(acc, ad, dbl + 2 * kk, idesc, 1u);
+                            if (C::NAT == 2)  // 3-bit: the weight panel's lo part against B hi (and lo when cat)
                                 mma_f16(acc, ad + (uint64_t)((NA * C::A_BYTES) >> 4), dbh + 2 * kk, idesc, 1u);
                         }
                     }
@@ -428,28 +439,30 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             mbar_drain(smem_u32(drain), 0, abort_flag);
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 2 + C::UNPACK / 32) {
         // ----------------------------------------------------------- unpack
-        const int r = tid - 64;  // weight row of the tile
+        // thread u: row r = u % 128 of the tile and PIECES of the stage's (matrix,
+        // K-block) pieces, piece index = (u / 128) * PIECES + pi, matrix = index / 2
+        const int u = tid - 64, r = u & 127, part = u >> 7;
+        constexpr int WPT = C::PIECES;
         MOEQ_GW_DECL;
         int rs = 0, s = 0;
         uint32_t rph = 0, ph = 0;
         bool ok = true;
         for (int g = 0; g < G && ok; ++g) {
             if (!MOEQ_GW(7, mbar_wait(smem_u32(&raw_full[rs]), rph, abort_flag, wl))) break;
-            if (r == 0 && g % nk == 0) MOEQ_TL_TAG(TLK, 5, ((unsigned)(g / nk) << 8) | blockIdx.x);
+            if (u == 0 && g % nk == 0) MOEQ_TL_TAG(TLK, 5, ((unsigned)(g / nk) << 8) | blockIdx.x);
             const unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
-            uint32_t cw[NA][2][BITS];
-            uint16_t sbits[NA][2];
+            uint32_t cw[WPT][BITS];
+            uint16_t sbits[WPT];
 #pragma unroll
-            for (int m = 0; m < NA; ++m)
+            for (int pi = 0; pi < WPT; ++pi) {
+                const int pc = part * WPT + pi, m = pc >> 1, b = pc & 1;
+                const uint32_t *cp = reinterpret_cast<const uint32_t *>(rw + ((m * 2 + b) * kGmM + r) * BPB);
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const uint32_t *cp = reinterpret_cast<const uint32_t *>(rw + ((m * 2 + b) * kGmM + r) * BPB);
-#pragma unroll
-                    for (int i = 0; i < BITS; ++i) cw[m][b][i] = cp[i];
-                    sbits[m][b] = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + r) * 2);
-                }
+                for (int i = 0; i < BITS; ++i) cw[pi][i] = cp[i];
+                sbits[pi] = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + r) * 2);
+            }
             mbar_arrive(smem_u32(&raw_empty[rs]));
             if (++rs == R) {
                 rs = 0;
@@ -458,68 +471,66 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             if (!MOEQ_GW(8, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag, wl))) break;
             unsigned char *sb = slots + (size_t)s * C::SLOT_BYTES;
 #pragma unroll
-            for (int m = 0; m < NA; ++m) {
+            for (int pi = 0; pi < WPT; ++pi) {
+                const int pc = part * WPT + pi, m = pc >> 1, b = pc & 1;
                 const uint32_t at = smem_u32(sb + m * C::A_BYTES);
+                const __half sc = __ushort_as_half(sbits[pi]);
+                if (BITS == 2) {
+                    const __half m2 = __hmul(sc, __float2half(-2.0f)), m1 = __hneg(sc);
+                    const uint32_t lut_lo = (uint32_t)__half_as_ushort(m2) | ((uint32_t)__half_as_ushort(m1) << 16);
+                    const uint32_t lut_hi = (uint32_t)__half_as_ushort(sc) << 16;  // {0, s}
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const __half sc = __ushort_as_half(sbits[m][b]);
-                    if (BITS == 2) {
-                        const __half m2 = __hmul(sc, __float2half(-2.0f)), m1 = __hneg(sc);
-                        const uint32_t lut_lo = (uint32_t)__half_as_ushort(m2) | ((uint32_t)__half_as_ushort(m1) << 16);
-                        const uint32_t lut_hi = (uint32_t)__half_as_ushort(sc) << 16;  // {0, s}
+                    for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 8 elements = 2 code bytes
+                        const uint32_t word = cw[pi][c >> 1];
+                        const uint32_t d0 = (word >> (16 * (c & 1))) & 0xffu;
+                        const uint32_t d1 = (word >> (16 * (c & 1) + 8)) & 0xffu;
+                        const uint32_t q0 = lut_pair(lut_lo, lut_hi, (d0 & 3u) | ((d0 & 0xCu) << 6));
+                        const uint32_t q1 = lut_pair(lut_lo, lut_hi, ((d0 >> 4) & 3u) | ((d0 & 0xC0u) << 2));
+                        const uint32_t q2 = lut_pair(lut_lo, lut_hi, (d1 & 3u) | ((d1 & 0xCu) << 6));
+                        const uint32_t q3 = lut_pair(lut_lo, lut_hi, ((d1 >> 4) & 3u) | ((d1 & 0xC0u) << 2));
+                        st_shared_v4(at + sw128_off(r, 4 * b + c), q0, q1, q2, q3);
+                    }
+                } else {
+                    // 3-bit levels -4..3 times s: v = level * s is exact in fp32; hi = fp16(v)
+                    // and lo = v - hi (exact in fp16) go to the hi and lo panels
+                    const float sf = __half2float(sc);
+                    const uint32_t at_lo = smem_u32(sb + (NA + m) * C::A_BYTES);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 8 elements = 2 code bytes
-                            const uint32_t word = cw[m][b][c >> 1];
-                            const uint32_t d0 = (word >> (16 * (c & 1))) & 0xffu;
-                            const uint32_t d1 = (word >> (16 * (c & 1) + 8)) & 0xffu;
-                            const uint32_t q0 = lut_pair(lut_lo, lut_hi, (d0 & 3u) | ((d0 & 0xCu) << 6));
-                            const uint32_t q1 = lut_pair(lut_lo, lut_hi, ((d0 >> 4) & 3u) | ((d0 & 0xC0u) << 2));
-                            const uint32_t q2 = lut_pair(lut_lo, lut_hi, (d1 & 3u) | ((d1 & 0xCu) << 6));
-                            const uint32_t q3 = lut_pair(lut_lo, lut_hi, ((d1 >> 4) & 3u) | ((d1 & 0xC0u) << 2));
-                            st_shared_v4(at + sw128_off(r, 4 * b + c), q0, q1, q2, q3);
-                        }
-                    } else {
-                        // 3-bit levels -4..3 times s: v = level * s is exact in fp32; hi = fp16(v)
-                        // and lo = v - hi (exact in fp16) go to the hi and lo panels
-                        const float sf = __half2float(sc);
-                        const uint32_t at_lo = smem_u32(sb + (NA + m) * C::A_BYTES);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t qv[4], lv[4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t qv[4], lv[4];
+                        for (int h2 = 0; h2 < 4; ++h2) {
+                            __half hv[2], lo[2];
 #pragma unroll
-                            for (int h2 = 0; h2 < 4; ++h2) {
-                                __half hv[2], lo[2];
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    const int i = 8 * c + 2 * h2 + u, off = 3 * i, wi = off >> 5, sh = off & 31;
-                                    const uint32_t lo_w = cw[m][b][wi];
-                                    const uint32_t hi_w = wi + 1 < BITS ? cw[m][b][wi + 1] : 0u;
-                                    const int code = (int)(__funnelshift_r(lo_w, hi_w, sh) & 7u);
-                                    const float v = (float)(code - 4) * sf;
-                                    hv[u] = __float2half_rn(v);
-                                    lo[u] = __float2half_rn(v - __half2float(hv[u]));
-                                }
-                                qv[h2] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
-                                lv[h2] = (uint32_t)__half_as_ushort(lo[0]) | ((uint32_t)__half_as_ushort(lo[1]) << 16);
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int i = 8 * c + 2 * h2 + e2, off = 3 * i, wi = off >> 5, sh = off & 31;
+                                const uint32_t lo_w = cw[pi][wi];
+                                const uint32_t hi_w = wi + 1 < BITS ? cw[pi][wi + 1] : 0u;
+                                const int code = (int)(__funnelshift_r(lo_w, hi_w, sh) & 7u);
+                                const float v = (float)(code - 4) * sf;
+                                hv[e2] = __float2half_rn(v);
+                                lo[e2] = __float2half_rn(v - __half2float(hv[e2]));
                             }
-                            st_shared_v4(at_lo + sw128_off(r, 4 * b + c), lv[0], lv[1], lv[2], lv[3]);
-                            st_shared_v4(at + sw128_off(r, 4 * b + c), qv[0], qv[1], qv[2], qv[3]);
+                            qv[h2] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+                            lv[h2] = (uint32_t)__half_as_ushort(lo[0]) | ((uint32_t)__half_as_ushort(lo[1]) << 16);
                         }
+                        st_shared_v4(at_lo + sw128_off(r, 4 * b + c), lv[0], lv[1], lv[2], lv[3]);
+                        st_shared_v4(at + sw128_off(r, 4 * b + c), qv[0], qv[1], qv[2], qv[3]);
                     }
                 }
             }
             fence_proxy_async();
             mbar_arrive(smem_u32(&a_full[s]));
-            if (r == 0 && g % nk == nk - 1) MOEQ_TL_TAG(TLK, 6, ((unsigned)(g / nk) << 8) | blockIdx.x);
+            if (u == 0 && g % nk == nk - 1) MOEQ_TL_TAG(TLK, 6, ((unsigned)(g / nk) << 8) | blockIdx.x);
             if (++s == S) {
                 s = 0;
                 ph ^= 1;
             }
         }
-        if (r == 0) MOEQ_GW_FLUSH(7, 9, 9);
+        if (u == 0) MOEQ_GW_FLUSH(7, 9, 9);
     } else {
         // --------------------------------------------------------- epilogue
-        const int et = tid - 192;                 // 0..127: table entry this thread loads
+        const int et = tid - 64 - C::UNPACK;      // 0..127: table entry this thread loads
         const int row = 32 * (warp & 3) + lane;   // accumulator lane = weight row
         const uint32_t tl_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         MOEQ_GW_DECL;
@@ -555,12 +566,25 @@ __global__ void __launch_bounds__(320, 1) ffn_gemm_kernel(const __grid_constant_
             if (et == 0) MOEQ_TL_TAG(TLK, 3, ((unsigned)j << 8) | blockIdx.x);
             const int *etab = s_exp + buf * kGmN;
             const uint32_t acc = tl_lane + (uint32_t)(buf * C::ACC_COLS);
+            const bool cat = nround <= kGmN / 2;  // lo products in columns [nround, 2 nround) (MMA warp)
             for (int c0 = 0; c0 < nround; c0 += 16) {
                 float acc0[16];
                 tmem_ld16(acc + (uint32_t)c0, acc0);
+                if (cat) {
+                    float lo0[16];
+                    tmem_ld16(acc + (uint32_t)(nround + c0), lo0);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) acc0[jj] += lo0[jj];
+                }
                 if (GATEUP) {
                     float acc1[16];
                     tmem_ld16(acc + (uint32_t)(kGmN + c0), acc1);
+                    if (cat) {
+                        float lo1[16];
+                        tmem_ld16(acc + (uint32_t)(kGmN + nround + c0), lo1);
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) acc1[jj] += lo1[jj];
+                    }
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int jc = c0 + jj;

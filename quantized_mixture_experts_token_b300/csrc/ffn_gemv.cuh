@@ -209,12 +209,15 @@ __device__ __forceinline__ bool gemv_unit(const GemvArgs &a, int u, int *tok, fl
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (a.route_mode == 1) {
         const int T = a.T, k = a.k, E = a.E;
+        MOEQ_TL(2, 10);
         if (warp < T) {
             const bool out = blockIdx.x == 0;
             warp_topk<PER>(a.logits + (size_t)warp * E, E, k, out ? a.idx_out + (size_t)warp * k : nullptr,
                            out ? a.w_out + (size_t)warp * k : nullptr, s_sel[warp], s_w[warp]);
         }
+        MOEQ_TL(2, 11);
         __syncthreads();
+        MOEQ_TL(2, 12);
         pb = 0;
         if (T == 1) {
             if (u >= k) return false;

@@ -82,7 +82,11 @@ constexpr int kExpertGemvMaxT = 512;
 // Token count up to which the decode fast path fuses routing and permutation.
 constexpr int kFusedRouteMaxT = kFusedMaxT;  // (the router kernel's tail handles up to 64 tokens)
 // Token count up to which every expert CTA ranks the router logits itself.
+#ifdef MOEQ_INCTA_ROUTE_MAXT
+constexpr int kInCtaRouteMaxT = MOEQ_INCTA_ROUTE_MAXT;
+#else
 constexpr int kInCtaRouteMaxT = 2;
+#endif
 
 struct Layout {
     size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, chunk_count, chunk_base, units,

@@ -47,6 +47,7 @@ __device__ __forceinline__ void warp_topk(const float *row, int E, int k, int32_
     uint32_t lm = 0u;
 #pragma unroll
     for (int i = 0; i < PER; ++i) lm = max(lm, key[i]);
+    MOEQ_TL(9, 0);  // (tracing builds) the logits are in registers
     int gt = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) gt += __shfl_sync(0xffffffffu, lm, j) > lm;
@@ -328,6 +329,7 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
         else if (nt <= 8) route_reduce<8>(acc, part, warp, lane);
         else route_reduce<16>(acc, part, warp, lane);
         __syncthreads();
+        MOEQ_TL(1, 5);
         if (tid < kRouteRows * kRouteTok) {
             const int r = tid / kRouteTok, t = tid % kRouteTok;
             if (t < nt && r < nr) {
