@@ -53,10 +53,13 @@ VERIFY_T = 64  # 3-bit decode: a multi-token verify window
 PREFILL3_T = 16384  # 3-bit prefill chunk, uniform routing
 SWEEP_T = (8, 16, 32, 64, 128, 256, 512, 1024)  # token counts of the GEMV / grouped-GEMM crossover sweep
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# current kernel versions from one ncu capture, with its source; None until
-# the kernel in this tree has been captured
-DECODE_LAYER_TRAFFIC = dict(bytes=None, source="not captured for this kernel version")
-GEMM_GU_TRAFFIC = dict(bytes=None, source="not captured for this kernel version")
+# current kernel versions from one ncu --set full capture (profiles/), with
+# its source; set to None when a kernel changes until it is captured again
+DECODE_LAYER_TRAFFIC = dict(bytes=4.269056e6 + 9.927936e6,
+                            source=("ncu: route_gemv_kernel 4.27 MB + ffn_gemv_kernel 9.93 MB, one B=1 layer "
+                                    "(profiles/route_gemv_decode_T1.md, ffn_gemv_decode_T1.md)"))
+GEMM_GU_TRAFFIC = dict(bytes=694.342144e6 + 20.294912e6,
+                       source="ncu: ffn_gemm_kernel<1,2> 694.3 MB read + 20.3 MB written (profiles/ffn_gemm_gateup_prefill_4k.md)")
 
 
 # ------------------------------------------------------------------ helpers
@@ -264,6 +267,33 @@ def s8_peak_tops():
         if lib.moe_peak_mma_s8(20000, 4, ctypes.byref(v)) == 0:
             best = max(best, v.value)
     return best or None
+
+
+def run_peaks():
+    """--peaks: the tensor-path microbenchmarks of libmoeq_peaks, one JSON line.
+
+    mma.sync s8 throughput, and the cycles one tcgen05.mma (M = 128, K = 16,
+    fp16) costs its issuing thread at the N and the stage sizes the grouped
+    prefill GEMMs use (8 or 16 MMAs per K = 64 stage)."""
+    import ctypes
+
+    import torch
+
+    torch.cuda.init()
+    lib = ctypes.CDLL(os.path.join(ROOT, "quantized_mixture_experts_token_b300", "libmoeq_peaks.so"))
+    lib.moe_peak_umma_issue.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_double)]
+    rows = []
+    for n in (32, 64, 128, 256):
+        for per_stage in (8, 16):
+            for sync in (0, 1):
+                v = ctypes.c_double(0.0)
+                rc = lib.moe_peak_umma_issue(n, per_stage, sync, ctypes.byref(v))
+                if rc != 0:
+                    raise RuntimeError(f"moe_peak_umma_issue({n}, {per_stage}, {sync}) returned {rc}")
+                rows.append(dict(n=n, mma_per_stage=per_stage, pipeline_sync=bool(sync), cycles_per_mma=round(v.value, 1),
+                                 dense_cycles=round(128 * n * 16 / 8192, 1)))
+    print(json.dumps(dict(metric="tensor_path_microbenchmarks", s8_mma_sync_tops=s8_peak_tops(), umma_issue=rows,
+                          note="dense_cycles: the cycles an M=128 K=16 fp16 MMA takes at 8192 fp16 FMA per SM per cycle")))
 
 
 def distinct_experts(gpu, xs, Ws, layers, ws, nl):
@@ -582,7 +612,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-3bit", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--peaks", action="store_true", help="only run the tensor-path microbenchmarks")
     args = ap.parse_args(argv)
+    if args.peaks:
+        run_peaks()
+        return
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)

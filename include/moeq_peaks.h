@@ -24,6 +24,17 @@ extern "C" {
  */
 int moe_peak_mma_s8(int iters, int blocks_per_sm, double *tops_out);
 
+/*
+ * Cycles per tcgen05.mma (kind::f16, M = 128, N = n, K = 16) issued by one
+ * thread from operands resident in shared memory, one CTA per SM: groups of
+ * per_stage MMAs, and with with_sync != 0 what a pipelined GEMM adds per group
+ * (two mbarrier tests, a tcgen05 fence, a commit).  The grouped prefill GEMMs
+ * of libmoeq issue 8 or 16 MMAs per K = 64 stage.  n a multiple of 16 in
+ * [16, 256], per_stage in [1, 64].  Synchronises the device; returns 0, -1 on
+ * a bad argument, -5 on a CUDA error.  Allocates nothing.
+ */
+int moe_peak_umma_issue(int n, int per_stage, int with_sync, double *cycles_per_mma);
+
 #ifdef __cplusplus
 }
 #endif

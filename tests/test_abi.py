@@ -41,7 +41,7 @@ def test_peaks_library_exports_its_header():
     src = open(os.path.join(ROOT, "include", "moeq_peaks.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
-    assert names == ["moe_peak_mma_s8"]
+    assert names == ["moe_peak_mma_s8", "moe_peak_umma_issue"]
     import __graft_entry__
 
     __graft_entry__.build()
@@ -49,7 +49,9 @@ def test_peaks_library_exports_its_header():
     for n in names:
         assert hasattr(lib, n), n
     lib.moe_peak_mma_s8.argtypes = [C.c_int, C.c_int, C.c_void_p]
-    assert lib.moe_peak_mma_s8(0, 1, None) == -1  # argument check, nothing launched
+    assert lib.moe_peak_mma_s8(0, 1, None) == -1  # argument checks, nothing launched
+    lib.moe_peak_umma_issue.argtypes = [C.c_int, C.c_int, C.c_int, C.c_void_p]
+    assert lib.moe_peak_umma_issue(24, 8, 1, None) == -1
 
 
 def test_workspace_bytes_host_logic(L):
