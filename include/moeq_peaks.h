@@ -26,12 +26,14 @@ int moe_peak_mma_s8(int iters, int blocks_per_sm, double *tops_out);
 
 /*
  * Cycles per tcgen05.mma (kind::f16, M = 128, N = n, K = 16) issued by one
- * thread from operands resident in shared memory, one CTA per SM: groups of
- * per_stage MMAs, and with with_sync != 0 what a pipelined GEMM adds per group
- * (two mbarrier tests, a tcgen05 fence, a commit).  The grouped prefill GEMMs
- * of libmoeq issue 8 or 16 MMAs per K = 64 stage.  n a multiple of 16 in
- * [16, 256], per_stage in [1, 64].  Synchronises the device; returns 0, -1 on
- * a bad argument, -5 on a CUDA error.  Allocates nothing.
+ * thread from operands resident in shared memory, one CTA per SM, in the order
+ * the grouped prefill GEMMs of libmoeq issue them: per K = 16 step both
+ * M = 128 blocks (two TMEM accumulators of n columns), times two B images when
+ * per_stage = 16 (the hi and lo halves of a split operand); 8 or 16 MMAs per
+ * K = 64 stage.  with_sync != 0 adds what a pipelined GEMM does per stage (two
+ * mbarrier tests, a tcgen05 fence, a commit).  n a multiple of 16 in [16, 256],
+ * per_stage 8 or 16.  Synchronises the device; returns 0, -1 on a bad argument,
+ * -5 on a CUDA error.  Allocates no device memory.
  */
 int moe_peak_umma_issue(int n, int per_stage, int with_sync, double *cycles_per_mma);
 

@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(256) mma_s8_loop(int iters, int seed) {
 
 // ---- tcgen05.mma issue cost: M = 128, K = 16, fp16, one issuing thread.
 __device__ long long g_umma_cycles;
+constexpr int kUmmaBytes = 2 * 16384 + 2 * 32768;  // two 128 x 64 A blocks, two 256 x 64 B images (fp16)
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -62,16 +63,20 @@ __device__ __forceinline__ bool mbar_try_once(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Thread 0 issues `stages` groups of `per_stage` MMAs (N = n) from resident
-// operands; with_sync adds what a pipelined GEMM does per stage: two tests of
-// (already completed) mbarriers, a tcgen05 fence and a commit.
-__global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int per_stage, int with_sync) {
+// Thread 0 issues `stages` groups of PER_STAGE MMAs (N = n) from resident
+// operands in the order the grouped GEMM uses: for each K = 16 step, both
+// M = 128 blocks (two accumulators), and with PER_STAGE = 16 a second B image
+// (the lo half of a split operand).  with_sync adds what a pipelined GEMM does
+// per stage: two tests of (already completed) mbarriers, a tcgen05 fence and a
+// commit.
+template <int PER_STAGE>
+__global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int with_sync) {
     extern __shared__ unsigned char raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t full, slot_free, fin;
     __shared__ uint32_t tslot;
     const int tid = threadIdx.x, warp = tid >> 5;
-    for (int i = tid; i < (16384 + 32768) / 4; i += blockDim.x) reinterpret_cast<uint32_t *>(sm)[i] = 0x3C003C00u * ((i & 7) == 0);
+    for (int i = tid; i < kUmmaBytes / 4; i += blockDim.x) reinterpret_cast<uint32_t *>(sm)[i] = 0x3C003C00u * ((i & 7) == 0);
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&full)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&slot_free)));
@@ -80,7 +85,7 @@ __global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(su32(&tslot)) : "memory");
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&tslot)) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -89,7 +94,8 @@ __global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tm = tslot;
     if (tid == 0) {
-        const uint64_t da = sw128_kmajor_desc(su32(sm)), db = sw128_kmajor_desc(su32(sm + 16384));
+        const uint64_t da = sw128_kmajor_desc(su32(sm)), db = sw128_kmajor_desc(su32(sm + 2 * 16384));
+        constexpr uint64_t kA = 16384 >> 4, kB = 32768 >> 4;  // descriptor strides of an A block and a B image
         const uint32_t idesc = (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
         const long long t0 = clock64();
         for (int g = 0; g < stages; ++g) {
@@ -97,20 +103,23 @@ __global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int
                 if (!(mbar_try_once(su32(&full), 0) && mbar_try_once(su32(&full), 0))) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             }
-            for (int i = 0; i < per_stage; ++i) {
-                const int kk = i & 3;
-                asm volatile(
-                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tm),
-                    "l"(da + 2 * kk), "l"(db + 2 * kk), "r"(idesc), "r"(1)
-                    : "memory");
-            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int h = 0; h < PER_STAGE / 8; ++h)
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tm + (uint32_t)(m * n)),
+                            "l"(da + m * kA + 2 * kk), "l"(db + h * kB + 2 * kk), "r"(idesc), "r"(1)
+                            : "memory");
             if (with_sync)
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(&slot_free))
                              : "memory");
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(&fin)) : "memory");
-        bool ok = false;  // the MMAs end within a millisecond; give up after about two seconds
+        bool ok = false;  // the MMAs end within a few milliseconds; give up after about two seconds
         for (const long long tw = clock64(); !ok && clock64() - tw < 4000000000ll;) ok = mbar_try_once(su32(&fin), 0);
         if (blockIdx.x == 0) g_umma_cycles = ok ? clock64() - t0 : -1;
     }
@@ -118,21 +127,26 @@ __global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int
     __syncthreads();
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tm) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tm) : "memory");
     }
 }
 
 }  // namespace
 
 extern "C" int moe_peak_umma_issue(int n, int per_stage, int with_sync, double *cycles_per_mma) {
-    if (!cycles_per_mma || n < 16 || n > 256 || n % 16 || per_stage < 1 || per_stage > 64) return -1;
+    if (!cycles_per_mma || n < 16 || n > 256 || n % 16 || (per_stage != 8 && per_stage != 16)) return -1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -5;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -5;
-    const int smem = 120 * 1024;  // 49 KB used; the rest keeps one CTA on each SM
-    if (cudaFuncSetAttribute(umma_issue_loop, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -5;
+    const int smem = 1024 + kUmmaBytes + 24 * 1024;  // the spare 24 KB keeps one CTA on each SM
     const int stages = 4096 / per_stage + 1;
-    umma_issue_loop<<<sms, 128, smem>>>(n, stages, per_stage, with_sync);
+    if (per_stage == 8) {
+        if (cudaFuncSetAttribute(umma_issue_loop<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -5;
+        umma_issue_loop<8><<<sms, 128, smem>>>(n, stages, with_sync);
+    } else {
+        if (cudaFuncSetAttribute(umma_issue_loop<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -5;
+        umma_issue_loop<16><<<sms, 128, smem>>>(n, stages, with_sync);
+    }
     long long cyc = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return -5;
     if (cudaMemcpyFromSymbol(&cyc, g_umma_cycles, sizeof cyc) != cudaSuccess || cyc <= 0) return -5;
