@@ -211,9 +211,9 @@ __device__ __forceinline__ bool gemv_unit(const GemvArgs &a, int u, int *tok, fl
         const int T = a.T, k = a.k, E = a.E;
         MOEQ_TL(2, 10);
         if (warp < T) {
-            const bool out = blockIdx.x == 0;
-            warp_topk<PER>(a.logits + (size_t)warp * E, E, k, out ? a.idx_out + (size_t)warp * k : nullptr,
-                           out ? a.w_out + (size_t)warp * k : nullptr, s_sel[warp], s_w[warp]);
+            const bool out = blockIdx.x == 0;  // the routing outputs are optional (NULL: not written)
+            warp_topk<PER>(a.logits + (size_t)warp * E, E, k, out && a.idx_out ? a.idx_out + (size_t)warp * k : nullptr,
+                           out && a.w_out ? a.w_out + (size_t)warp * k : nullptr, s_sel[warp], s_w[warp]);
         }
         MOEQ_TL(2, 11);
         __syncthreads();

@@ -98,6 +98,23 @@ def test_layer_forward_two_tokens(full, cuda_lib, same):
     assert cuda_lib.device_status() == 0
 
 
+@pytest.mark.parametrize("T", [1, 2])
+def test_layer_forward_without_routing_outputs(full, cuda_lib, T):
+    """The routing outputs of moe_layer_forward are optional: with none asked
+    for, the in-CTA routing (T <= 2) writes nothing for any token and y is the
+    same as with them."""
+    x = full.x(T, seed=610).to(_dev())
+    ws = _ws(cuda_lib, T, full.shape)
+    y_with, _, _ = cuda_lib.layer_forward(x, full.W, full.dev.Wr, None, full.shape.k, ws, want_routing=True)
+    y_without = cuda_lib.layer_forward(x, full.W, full.dev.Wr, None, full.shape.k, ws)
+    torch.cuda.synchronize()
+    ref = full.oracle(x.cpu())
+    full.check_y(y_without.cpu().numpy(), ref, delta=DELTA[1])
+    # the same kernels on the same inputs; only the fp32 atomics' order may differ
+    assert np.allclose(y_with.cpu().numpy(), y_without.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    assert cuda_lib.device_status() == 0
+
+
 # ------------------------------------------- a decode stack inside a CUDA graph
 
 
