@@ -11,19 +11,25 @@
 //     reach +-3, whose product needs up to 13 significant bits, so the 3-bit
 //     panel is split into fp16 hi + lo (lo exact: at most 2 significant bits)
 //     and each product takes a third MMA, A_lo * B_hi (A_lo * B_lo, ~2^-22
-//     relative, is dropped like the rest of the B split's residue);
-//   * B (activations, N = up to 128 sorted tokens): v = q * s_a * 2^-e split
+//     relative, is dropped like the rest of the B split's residue).  The
+//     panel lives in tensor memory (the MMA's A operand from TMEM), written by
+//     the unpack warps with tcgen05.st: the tcgen05 ordering rules (commit ->
+//     mbarrier -> fence) then cover its reuse.  Ordinary shared-memory stores
+//     into an operand slot released by a tcgen05.commit were measured to race
+//     with the tensor core's reads of that slot;
+//   * B (activations, N = up to TILE_N sorted tokens): v = q * s_a * 2^-e split
 //     into fp16 hi + lo (hi + lo == v to ~2^-22), two MMAs into one fp32
 //     accumulator, so the per-32-block activation scale is carried without an
 //     epilogue per K-block;
 //   * e is a per-row power of two, undone exactly in the epilogue.
 //
-// Work item = (tile of <= 128 sorted pairs of one expert, 128-row block of its
-// weight matrix); the epilogue reads the accumulator (lane = weight row):
+// Work item = (tile of <= TILE_N sorted pairs of one expert, 128-row block of
+// its weight matrix); the epilogue reads the accumulator (lane = weight row):
 //   gate/up: h = silu(G) * U and int8 re-quantisation per 32 rows (one warp =
 //            one quantisation block), stored as q_h, s_h;
-//   down:    D * 2^e, weighted by the routing weight and added into y
-//            (fp32 atomics), or stored per sorted pair.
+//   down:    D * 2^e, weighted by the routing weight and added into y with
+//            one 128-byte bulk reduction per pair and 32 rows, or stored per
+//            sorted pair.
 // The kernel is persistent and warp-specialised (see ffn_gemm_kernel).
 #pragma once
 
@@ -32,16 +38,16 @@
 
 namespace moeq {
 
-constexpr int kGmM = 128;  // MMA M: weight rows per CTA
-constexpr int kGmN = 128;  // max tokens per tile (MMA N)
+constexpr int kGmM = 128;  // MMA M: weight rows per CTA (= TMEM lanes)
 constexpr int kGmK = 64;   // K per pipeline stage = one 128-byte swizzle row of fp16
+constexpr int kTmemCols = 512;
 
 struct GemmArgs {
     int T, H, I, E, k;
     const uint8_t *codes[3];
     const uint16_t *scales[3];
     const Tile *tiles;
-    const int *ctrl;  // ctrl[2] = number of tiles
+    const int *ntiles;  // number of tiles (written by the plan kernel)
     const int32_t *perm_tok, *perm_slot;
     const float *w;
     // B operand image (fp16, see split_rows_kernel): [K/64][hi, lo][bimg_rows][64],
@@ -88,6 +94,29 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// D (TMEM) (+)= A (TMEM: lane = row, 8 columns = 16 fp16 of K) * B (shared memory).
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -149,34 +178,43 @@ template <bool GATEUP, int BITS>
 struct GemmCfg {
     static constexpr int NA = GATEUP ? 2 : 1;  // weight matrices per work item (gate + up, or down)
     static constexpr int BPB = 4 * BITS;
-    // operand ring, K = 64 per stage (MOEQ_GEMM_STAGES overrides the depth at build time)
-#if defined(MOEQ_GEMM_STAGES_GU) && defined(MOEQ_GEMM_STAGES_DN)
-    static constexpr int STAGES = GATEUP ? MOEQ_GEMM_STAGES_GU : MOEQ_GEMM_STAGES_DN;
-#elif defined(MOEQ_GEMM_STAGES)
+    static constexpr int NAT = BITS == 3 ? 2 : 1;  // weight panels per matrix: hi (, lo)
+    // tokens per tile (MMA N): TMEM holds two accumulator buffers of NA x TILE_N
+    // columns and PSTAGES weight panels of NAT x NA x 32 columns (K = 64 fp16)
+    static constexpr int TILE_N = GATEUP ? (BITS == 2 ? 96 : 64) : 128;
+    static constexpr int ACC_COLS = NA * TILE_N;           // one accumulator buffer (fp32 columns)
+    static constexpr int A_COLS = NAT * NA * (kGmK / 2);   // one stage of weight panels
+    static constexpr int A_BASE = 2 * ACC_COLS;            // first panel column
+#if defined(MOEQ_GEMM_PSTAGES)
+    static constexpr int PSTAGES = MOEQ_GEMM_PSTAGES;
+#else
+    static constexpr int PSTAGES = (kTmemCols - A_BASE) / A_COLS > 4 ? 4 : (kTmemCols - A_BASE) / A_COLS;
+#endif
+    // token-row ring in shared memory, refilled by bulk copies (MOEQ_GEMM_STAGES overrides)
+#if defined(MOEQ_GEMM_STAGES)
     static constexpr int STAGES = MOEQ_GEMM_STAGES;
 #else
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = GATEUP ? 6 : 5;
 #endif
-    static constexpr int RSTAGES = (GATEUP && BITS == 3) ? 4 : 6;  // raw-code ring (runs further ahead)
-    static constexpr int A_BYTES = kGmM * kGmK * 2;                // fp16 weight tile
-    static constexpr int NAT = BITS == 3 ? 2 : 1;                  // weight tiles per matrix: hi (, lo)
-    static constexpr int B_BYTES = kGmN * kGmK * 2;                // fp16 activation tile (hi or lo)
-    static constexpr int SLOT_BYTES = NAT * NA * A_BYTES + 2 * B_BYTES;  // A [part][matrix], then B hi, lo
+    static constexpr int RSTAGES = 6;                    // raw-code ring (runs further ahead)
+    static constexpr int B_BYTES = TILE_N * kGmK * 2;    // fp16 activation tile (hi or lo)
+    static constexpr int SLOT_BYTES = 2 * B_BYTES;       // B hi, lo
     static constexpr int RAW_CODES = NA * 2 * kGmM * BPB;  // two K-blocks per stage
     static constexpr int RAW_SCALES = NA * 2 * kGmM * 2;
     static constexpr int RAW_BYTES = RAW_CODES + RAW_SCALES;
-    static constexpr int ACC_COLS = NA * kGmN;      // one accumulator buffer (fp32 columns)
-    static constexpr int TMEM_COLS = 2 * ACC_COLS;  // double buffered: 512 (gate/up) or 256 (down)
-    static constexpr int NUM_BARS = 2 * RSTAGES + 3 * STAGES + 5;
-    static constexpr int MISC_BYTES = 8 * NUM_BARS + 16 + 3 * 2 * kGmN * 4;
+    static constexpr int NUM_BARS = 2 * RSTAGES + 2 * STAGES + 2 * PSTAGES + 5;
+    static constexpr int MISC_BYTES = 8 * NUM_BARS + 16 + 3 * 2 * TILE_N * 4;
     // down: per epilogue warp two staging buffers of 16 tokens x its 32 rows of
     // w * D (fp32) that it adds into y with bulk reductions
     static constexpr int STAGE_BYTES = GATEUP ? 0 : 2 * 16 * kGmM * 4;
     static constexpr size_t SMEM =
         1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES + 128 + STAGE_BYTES;
-    static constexpr int UNPACK = 128;                   // unpack threads (warps 2 .. 2 + UNPACK/32 - 1)
+    static constexpr int UNPACK = 128;                   // unpack threads (warps 2 .. 5)
     static constexpr int THREADS = 64 + UNPACK + 128;    // producer, MMA, unpack, epilogue warps
-    static constexpr int PIECES = NA * 2 * 128 / UNPACK;  // (matrix, K-block) pieces per unpack thread and stage
+    static constexpr int PIECES = NA * 2;                // (matrix, K-block) pieces per unpack thread and stage
+    static_assert(PSTAGES >= 2 && A_BASE + PSTAGES * A_COLS <= kTmemCols, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(TILE_N % 16 == 0 && TILE_N >= kTileMin && TILE_N <= kTileMax && B_BYTES % 1024 == 0, "tile shape");
 };
 
 // Tracing builds: cycles each role spends in each wait, per CTA and kernel.
@@ -221,13 +259,17 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
 
 // Persistent grouped GEMM: one CTA per SM walks the work items q = blockIdx.x,
 // blockIdx.x + gridDim.x, ... where q = (tile, 128-row M block).  Each item is
-// K/64 pipeline stages; stage g of this CTA uses operand slot g % STAGES and
-// raw slot g % RSTAGES, so every role derives the same slot and phase from g.
+// K/64 pipeline stages; stage g of this CTA uses token slot g % STAGES, panel
+// stage g % PSTAGES and raw slot g % RSTAGES, so every role derives the same
+// slots and phases from g.
 //   warp 0     producer: bulk copies of the raw codes/scales (RSTAGES ahead)
 //              and of the tile's B rows (hi, lo: one contiguous, pre-swizzled
-//              run each per K stage) into the operand slots, on mbarriers
-//   warp 1     TMEM owner; lane 0 issues the MMAs (hi and lo per K step)
-//   warps 2-5  unpack: row r of the weight tile, codes -> fp16 level*scale
+//              run each per K stage) into the token slots, on mbarriers
+//   warp 1     TMEM owner; lane 0 issues the MMAs (A from TMEM, B from shared
+//              memory)
+//   warps 2-5  unpack: codes -> fp16 level*scale, written into the TMEM panel
+//              stage with tcgen05.st; warp w writes the 32 weight rows of its
+//              TMEM lane quadrant w % 4
 //   warps 6-9  epilogue on the other accumulator buffer (TMEM lane quadrant
 //              = warp % 4), so item i's epilogue overlaps item i+1's MMAs
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag,
@@ -235,29 +277,30 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
 template <bool GATEUP, int BITS>
 __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_kernel(const __grid_constant__ GemmArgs a) {
     using C = GemmCfg<GATEUP, BITS>;
-    constexpr int NA = C::NA, BPB = C::BPB, S = C::STAGES, R = C::RSTAGES;
+    constexpr int NA = C::NA, BPB = C::BPB, S = C::STAGES, R = C::RSTAGES, PS = C::PSTAGES, TN = C::TILE_N;
     const int MT = (GATEUP ? a.I : a.H) / kGmM;
     const int K = GATEUP ? a.H : a.I;
     const int KB = K / 32, nk = K / kGmK;
     const int NR = GATEUP ? a.I : a.H;  // rows of each weight matrix
-    const int n_items = a.ctrl[2] * MT;
+    const int n_items = *a.ntiles * MT;
     const int nq = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int G = nq * nk;  // pipeline stages of this CTA
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *slots = smem;                                       // S x SLOT_BYTES
+    unsigned char *slots = smem;                                       // S x SLOT_BYTES (B hi, lo)
     unsigned char *raws = smem + (size_t)S * C::SLOT_BYTES;            // R x RAW_BYTES
     uint64_t *bars = reinterpret_cast<uint64_t *>(raws + (size_t)R * C::RAW_BYTES);
     uint64_t *raw_full = bars, *raw_empty = bars + R;
-    uint64_t *a_full = bars + 2 * R, *b_full = a_full + S, *slot_empty = b_full + S;
-    uint64_t *acc_full = slot_empty + S, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+    uint64_t *b_full = bars + 2 * R, *b_empty = b_full + S;
+    uint64_t *a_full = b_empty + S, *a_empty = a_full + PS;
+    uint64_t *acc_full = a_empty + PS, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *s_tok = reinterpret_cast<int *>(tmem_slot + 4);  // [2][kGmN] per accumulator buffer
-    int *s_exp = s_tok + 2 * kGmN;
-    float *s_wt = reinterpret_cast<float *>(s_exp + 2 * kGmN);
-    float *s_stage = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_wt + 2 * kGmN) + 127) & ~(uintptr_t)127);
+    int *s_tok = reinterpret_cast<int *>(tmem_slot + 4);  // [2][TN] per accumulator buffer
+    int *s_exp = s_tok + 2 * TN;
+    float *s_wt = reinterpret_cast<float *>(s_exp + 2 * TN);
+    float *s_stage = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_wt + 2 * TN) + 127) & ~(uintptr_t)127);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t wl = wait_limit();
@@ -268,9 +311,12 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             mbar_init(smem_u32(&raw_empty[i]), C::UNPACK);
         }
         for (int i = 0; i < S; ++i) {
-            mbar_init(smem_u32(&a_full[i]), C::UNPACK);
             mbar_init(smem_u32(&b_full[i]), 1);
-            mbar_init(smem_u32(&slot_empty[i]), 1);
+            mbar_init(smem_u32(&b_empty[i]), 1);
+        }
+        for (int i = 0; i < PS; ++i) {
+            mbar_init(smem_u32(&a_full[i]), C::UNPACK);
+            mbar_init(smem_u32(&a_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
@@ -282,7 +328,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(C::TMEM_COLS)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -346,15 +392,15 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                 if (!ok) break;
                 // B rows of this stage: hi/lo of sorted pairs p0 .. p0 + nround, K columns
                 // [64 ks, 64 ks + 64), one contiguous run of 128-byte rows per half
-                if (!__all_sync(0xffffffffu, MOEQ_GW(1, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag, wl)))) {
+                if (!__all_sync(0xffffffffu, MOEQ_GW(1, mbar_wait(smem_u32(&b_empty[s]), ph ^ 1, abort_flag, wl)))) {
                     ok = false;
                     break;
                 }
                 const uint32_t bbar = smem_u32(&b_full[s]);
-                // tiles of <= kGmN/2 rows: the lo rows follow the hi rows, so that one MMA
+                // tiles of <= TILE_N/2 rows: the lo rows follow the hi rows, so that one MMA
                 // of N = 2 nround forms both products (see the MMA warp)
-                const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES + C::NAT * NA * C::A_BYTES),
-                               blo = nround <= kGmN / 2 ? bhi + (uint32_t)(nround * 128) : bhi + C::B_BYTES;
+                const uint32_t bhi = smem_u32(slots + (size_t)s * C::SLOT_BYTES),
+                               blo = nround <= TN / 2 ? bhi + (uint32_t)(nround * 128) : bhi + C::B_BYTES;
                 if (lane == 0) mbar_arrive_expect_tx(bbar, (uint32_t)(2 * nround * kGmK * 2));
                 __syncwarp();
                 if (lane < 2)
@@ -379,22 +425,23 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
             MOEQ_GW_DECL;
-            // descriptors: slot s, matrix m, K step kk = base + ((s*SLOT + m*A) >> 4) + 2 kk
+            // B descriptors: slot s, K step kk = base + ((s * SLOT) >> 4) + 2 kk;
+            // A in TMEM: panel stage ps, matrix m, K step kk at column
+            // A_BASE + ps A_COLS + m 32 + 8 kk (lo panel of 3-bit: + NA 32)
             const uint64_t d0 = sw128_desc(smem_u32(slots));
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, ps = 0;
+            uint32_t ph = 0, pph = 0;
             bool ok = true;
             Tile next = nq > 0 ? item_tile(0) : Tile{};
             for (int j = 0; j < nq && ok; ++j) {
                 const Tile tl = next;
                 if (j + 1 < nq) next = item_tile(j + 1);  // consumed one item later
-                // a tile of nround <= kGmN / 2 rows has B = [hi rows; lo rows] and takes one MMA
-                // of N = 2 nround per product: hi into accumulator columns [0, nround), lo into
-                // [nround, 2 nround), added in the epilogue (an MMA costs about the same down
-                // to N = 64, so this halves the time of small tiles); larger tiles take two MMAs
+                // a tile of nround <= TILE_N / 2 rows has B = [hi rows; lo rows] and takes one
+                // MMA of N = 2 nround per product: hi into accumulator columns [0, nround), lo
+                // into [nround, 2 nround), added in the epilogue; larger tiles take two MMAs
                 // (hi, lo) into the same columns
                 const int nround = (tl.n + 15) & ~15;
-                const bool cat = nround <= kGmN / 2;
+                const bool cat = nround <= TN / 2;
                 const uint32_t idesc = f16_idesc(kGmM, cat ? 2 * nround : nround);
                 const int buf = j & 1;
                 if (!MOEQ_GW(3, mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag, wl))) break;
@@ -402,32 +449,37 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                 tc_fence_after();
                 const uint32_t acc0 = tmem + (uint32_t)(buf * C::ACC_COLS);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!MOEQ_GW(4, mbar_wait(smem_u32(&a_full[s]), ph, abort_flag, wl)) ||
+                    if (!MOEQ_GW(4, mbar_wait(smem_u32(&a_full[ps]), pph, abort_flag, wl)) ||
                         !MOEQ_GW(5, mbar_wait(smem_u32(&b_full[s]), ph, abort_flag, wl))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (ks == 0) MOEQ_TL_TAG(TLK, 1, ((unsigned)j << 8) | blockIdx.x);
-                    const uint64_t ds = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
-                    const uint64_t dbh = ds + (uint64_t)((C::NAT * NA * C::A_BYTES) >> 4);
+                    const uint64_t dbh = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
                     const uint64_t dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
+                    const uint32_t ap = tmem + (uint32_t)(C::A_BASE + ps * C::A_COLS);
 #pragma unroll
                     for (int kk = 0; kk < kGmK / 16; ++kk) {
 #pragma unroll
                         for (int m = 0; m < NA; ++m) {
-                            const uint64_t ad = ds + (uint64_t)((m * C::A_BYTES) >> 4) + 2 * kk;
-                            const uint32_t acc = acc0 + (uint32_t)(m * kGmN);
-                            mma_f16(acc, ad, dbh + 2 * kk, idesc, (ks | kk) != 0);
-                            if (!cat) mma_f16(acc, ad, dbl + 2 * kk, idesc, 1u);
+                            const uint32_t at = ap + (uint32_t)(m * (kGmK / 2) + 8 * kk);
+                            const uint32_t acc = acc0 + (uint32_t)(m * TN);
+                            mma_f16_ta(acc, at, dbh + 2 * kk, idesc, (ks | kk) != 0);
+                            if (!cat) mma_f16_ta(acc, at, dbl + 2 * kk, idesc, 1u);
                             if (C::NAT == 2)  // 3-bit: the weight panel's lo part against B hi (and lo when cat)
-                                mma_f16(acc, ad + (uint64_t)((NA * C::A_BYTES) >> 4), dbh + 2 * kk, idesc, 1u);
+                                mma_f16_ta(acc, at + (uint32_t)(NA * (kGmK / 2)), dbh + 2 * kk, idesc, 1u);
                         }
                     }
-                    mma_commit(smem_u32(&slot_empty[s]));
+                    mma_commit(smem_u32(&a_empty[ps]));
+                    mma_commit(smem_u32(&b_empty[s]));
                     if (++s == S) {
                         s = 0;
                         ph ^= 1;
+                    }
+                    if (++ps == PS) {
+                        ps = 0;
+                        pph ^= 1;
                     }
                 }
                 if (ok) mma_commit(smem_u32(&acc_full[buf]));
@@ -441,93 +493,94 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
         __syncwarp();
     } else if (warp < 2 + C::UNPACK / 32) {
         // ----------------------------------------------------------- unpack
-        // thread u: row r = u % 128 of the tile and PIECES of the stage's (matrix,
-        // K-block) pieces, piece index = (u / 128) * PIECES + pi, matrix = index / 2
-        const int u = tid - 64, r = u & 127, part = u >> 7;
+        // warp w writes TMEM lanes 32 (w % 4) .. + 31: thread = weight row r of the
+        // item's 128-row block, all (matrix, K-block) pieces of its row per stage
+        const int q = warp & 3, r = 32 * q + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)C::A_BASE;
         constexpr int WPT = C::PIECES;
         MOEQ_GW_DECL;
-        int rs = 0, s = 0;
-        uint32_t rph = 0, ph = 0;
+        int rs = 0, ps = 0;
+        uint32_t rph = 0, pph = 0;
         bool ok = true;
         for (int g = 0; g < G && ok; ++g) {
-            if (!MOEQ_GW(7, mbar_wait(smem_u32(&raw_full[rs]), rph, abort_flag, wl))) break;
-            if (u == 0 && g % nk == 0) MOEQ_TL_TAG(TLK, 5, ((unsigned)(g / nk) << 8) | blockIdx.x);
+            if (!__all_sync(0xffffffffu, MOEQ_GW(7, mbar_wait(smem_u32(&raw_full[rs]), rph, abort_flag, wl)))) break;
+            if (r == 0 && g % nk == 0) MOEQ_TL_TAG(TLK, 5, ((unsigned)(g / nk) << 8) | blockIdx.x);
             const unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
             uint32_t cw[WPT][BITS];
             uint16_t sbits[WPT];
 #pragma unroll
-            for (int pi = 0; pi < WPT; ++pi) {
-                const int pc = part * WPT + pi, m = pc >> 1, b = pc & 1;
-                const uint32_t *cp = reinterpret_cast<const uint32_t *>(rw + ((m * 2 + b) * kGmM + r) * BPB);
+            for (int pi = 0; pi < WPT; ++pi) {  // piece pi = (matrix pi / 2, K-block pi % 2)
+                const uint32_t *cp = reinterpret_cast<const uint32_t *>(rw + (pi * kGmM + r) * BPB);
 #pragma unroll
                 for (int i = 0; i < BITS; ++i) cw[pi][i] = cp[i];
-                sbits[pi] = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + ((m * 2 + b) * kGmM + r) * 2);
+                sbits[pi] = *reinterpret_cast<const uint16_t *>(rw + C::RAW_CODES + (pi * kGmM + r) * 2);
             }
             mbar_arrive(smem_u32(&raw_empty[rs]));
             if (++rs == R) {
                 rs = 0;
                 rph ^= 1;
             }
-            if (!MOEQ_GW(8, mbar_wait(smem_u32(&slot_empty[s]), ph ^ 1, abort_flag, wl))) break;
-            unsigned char *sb = slots + (size_t)s * C::SLOT_BYTES;
+            // the panel stage is free once the MMAs that read it have completed
+            if (!__all_sync(0xffffffffu, MOEQ_GW(8, mbar_wait(smem_u32(&a_empty[ps]), pph ^ 1, abort_flag, wl)))) break;
+            tc_fence_after();
+            const uint32_t tp = t_row + (uint32_t)(ps * C::A_COLS);
 #pragma unroll
-            for (int pi = 0; pi < WPT; ++pi) {
-                const int pc = part * WPT + pi, m = pc >> 1, b = pc & 1;
-                const uint32_t at = smem_u32(sb + m * C::A_BYTES);
-                const __half sc = __ushort_as_half(sbits[pi]);
-                if (BITS == 2) {
-                    const __half m2 = __hmul(sc, __float2half(-2.0f)), m1 = __hneg(sc);
-                    const uint32_t lut_lo = (uint32_t)__half_as_ushort(m2) | ((uint32_t)__half_as_ushort(m1) << 16);
-                    const uint32_t lut_hi = (uint32_t)__half_as_ushort(sc) << 16;  // {0, s}
+            for (int m = 0; m < NA; ++m) {
+                uint32_t hv[32], lv[32];  // the row's 64 K values of matrix m: K-block 0 then 1, 2 fp16 per word
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {  // 16-byte chunk = 8 elements = 2 code bytes
-                        const uint32_t word = cw[pi][c >> 1];
-                        const uint32_t d0 = (word >> (16 * (c & 1))) & 0xffu;
-                        const uint32_t d1 = (word >> (16 * (c & 1) + 8)) & 0xffu;
-                        const uint32_t q0 = lut_pair(lut_lo, lut_hi, (d0 & 3u) | ((d0 & 0xCu) << 6));
-                        const uint32_t q1 = lut_pair(lut_lo, lut_hi, ((d0 >> 4) & 3u) | ((d0 & 0xC0u) << 2));
-                        const uint32_t q2 = lut_pair(lut_lo, lut_hi, (d1 & 3u) | ((d1 & 0xCu) << 6));
-                        const uint32_t q3 = lut_pair(lut_lo, lut_hi, ((d1 >> 4) & 3u) | ((d1 & 0xC0u) << 2));
-                        st_shared_v4(at + sw128_off(r, 4 * b + c), q0, q1, q2, q3);
-                    }
-                } else {
-                    // 3-bit levels -4..3 times s: v = level * s is exact in fp32; hi = fp16(v)
-                    // and lo = v - hi (exact in fp16) go to the hi and lo panels
-                    const float sf = __half2float(sc);
-                    const uint32_t at_lo = smem_u32(sb + (NA + m) * C::A_BYTES);
+                for (int b = 0; b < 2; ++b) {
+                    const int pi = 2 * m + b;
+                    const __half sc = __ushort_as_half(sbits[pi]);
+                    if (BITS == 2) {
+                        const __half m2 = __hmul(sc, __float2half(-2.0f)), m1 = __hneg(sc);
+                        const uint32_t lut_lo = (uint32_t)__half_as_ushort(m2) | ((uint32_t)__half_as_ushort(m1) << 16);
+                        const uint32_t lut_hi = (uint32_t)__half_as_ushort(sc) << 16;  // {0, s}
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t qv[4], lv[4];
+                        for (int c = 0; c < 4; ++c) {  // 8 elements = 2 code bytes
+                            const uint32_t word = cw[pi][c >> 1];
+                            const uint32_t d0 = (word >> (16 * (c & 1))) & 0xffu;
+                            const uint32_t d1 = (word >> (16 * (c & 1) + 8)) & 0xffu;
+                            uint32_t *o = hv + 16 * b + 4 * c;
+                            o[0] = lut_pair(lut_lo, lut_hi, (d0 & 3u) | ((d0 & 0xCu) << 6));
+                            o[1] = lut_pair(lut_lo, lut_hi, ((d0 >> 4) & 3u) | ((d0 & 0xC0u) << 2));
+                            o[2] = lut_pair(lut_lo, lut_hi, (d1 & 3u) | ((d1 & 0xCu) << 6));
+                            o[3] = lut_pair(lut_lo, lut_hi, ((d1 >> 4) & 3u) | ((d1 & 0xC0u) << 2));
+                        }
+                    } else {
+                        // 3-bit levels -4..3 times s: v = level * s is exact in fp32; hi = fp16(v)
+                        // and lo = v - hi (exact in fp16) go to the hi and lo panels
+                        const float sf = __half2float(sc);
 #pragma unroll
-                        for (int h2 = 0; h2 < 4; ++h2) {
-                            __half hv[2], lo[2];
+                        for (int h2 = 0; h2 < 16; ++h2) {
+                            __half hh[2], ll[2];
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2) {
-                                const int i = 8 * c + 2 * h2 + e2, off = 3 * i, wi = off >> 5, sh = off & 31;
+                                const int i = 2 * h2 + e2, off = 3 * i, wi = off >> 5, sh = off & 31;
                                 const uint32_t lo_w = cw[pi][wi];
                                 const uint32_t hi_w = wi + 1 < BITS ? cw[pi][wi + 1] : 0u;
                                 const int code = (int)(__funnelshift_r(lo_w, hi_w, sh) & 7u);
                                 const float v = (float)(code - 4) * sf;
-                                hv[e2] = __float2half_rn(v);
-                                lo[e2] = __float2half_rn(v - __half2float(hv[e2]));
+                                hh[e2] = __float2half_rn(v);
+                                ll[e2] = __float2half_rn(v - __half2float(hh[e2]));
                             }
-                            qv[h2] = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
-                            lv[h2] = (uint32_t)__half_as_ushort(lo[0]) | ((uint32_t)__half_as_ushort(lo[1]) << 16);
+                            hv[16 * b + h2] = (uint32_t)__half_as_ushort(hh[0]) | ((uint32_t)__half_as_ushort(hh[1]) << 16);
+                            lv[16 * b + h2] = (uint32_t)__half_as_ushort(ll[0]) | ((uint32_t)__half_as_ushort(ll[1]) << 16);
                         }
-                        st_shared_v4(at_lo + sw128_off(r, 4 * b + c), lv[0], lv[1], lv[2], lv[3]);
-                        st_shared_v4(at + sw128_off(r, 4 * b + c), qv[0], qv[1], qv[2], qv[3]);
                     }
                 }
+                tmem_st32(tp + (uint32_t)(m * (kGmK / 2)), hv);
+                if (C::NAT == 2) tmem_st32(tp + (uint32_t)((NA + m) * (kGmK / 2)), lv);
             }
-            fence_proxy_async();
-            mbar_arrive(smem_u32(&a_full[s]));
-            if (u == 0 && g % nk == nk - 1) MOEQ_TL_TAG(TLK, 6, ((unsigned)(g / nk) << 8) | blockIdx.x);
-            if (++s == S) {
-                s = 0;
-                ph ^= 1;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&a_full[ps]));
+            if (r == 0 && g % nk == nk - 1) MOEQ_TL_TAG(TLK, 6, ((unsigned)(g / nk) << 8) | blockIdx.x);
+            if (++ps == PS) {
+                ps = 0;
+                pph ^= 1;
             }
         }
-        if (u == 0) MOEQ_GW_FLUSH(7, 9, 9);
+        if (r == 0) MOEQ_GW_FLUSH(7, 9, 9);
     } else {
         // --------------------------------------------------------- epilogue
         const int et = tid - 64 - C::UNPACK;      // 0..127: table entry this thread loads
@@ -540,7 +593,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             const Tile tl = item_tile(j);
             const int m0 = item_m0(j);
             const int buf = j & 1, p0 = tl.p0, nval = tl.n, nround = (nval + 15) & ~15;
-            {
+            if (et < TN) {
                 const int p = p0 + min(et, nval - 1);
                 int t = a.perm_tok[p];
                 const int js = a.perm_slot[p];
@@ -551,9 +604,9 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                 } else if (!GATEUP && a.w) {
                     wv = a.w[(size_t)t * a.k + js];
                 }
-                s_tok[buf * kGmN + et] = t;
-                s_exp[buf * kGmN + et] = a.brow_exp[p];
-                s_wt[buf * kGmN + et] = wv;
+                s_tok[buf * TN + et] = t;
+                s_exp[buf * TN + et] = a.brow_exp[p];
+                s_wt[buf * TN + et] = wv;
             }
             named_sync(1, 128);
             if (dead) continue;
@@ -564,9 +617,9 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             }
             tc_fence_after();
             if (et == 0) MOEQ_TL_TAG(TLK, 3, ((unsigned)j << 8) | blockIdx.x);
-            const int *etab = s_exp + buf * kGmN;
+            const int *etab = s_exp + buf * TN;
             const uint32_t acc = tl_lane + (uint32_t)(buf * C::ACC_COLS);
-            const bool cat = nround <= kGmN / 2;  // lo products in columns [nround, 2 nround) (MMA warp)
+            const bool cat = nround <= TN / 2;  // lo products in columns [nround, 2 nround) (MMA warp)
             for (int c0 = 0; c0 < nround; c0 += 16) {
                 float acc0[16];
                 tmem_ld16(acc + (uint32_t)c0, acc0);
@@ -578,10 +631,10 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                 }
                 if (GATEUP) {
                     float acc1[16];
-                    tmem_ld16(acc + (uint32_t)(kGmN + c0), acc1);
+                    tmem_ld16(acc + (uint32_t)(TN + c0), acc1);
                     if (cat) {
                         float lo1[16];
-                        tmem_ld16(acc + (uint32_t)(kGmN + nround + c0), lo1);
+                        tmem_ld16(acc + (uint32_t)(TN + nround + c0), lo1);
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) acc1[jj] += lo1[jj];
                     }
@@ -599,8 +652,8 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                         if (lane == 0) a.sh[p * (a.I / 32) + (m0 + row) / 32] = s;
                     }
                 } else {
-                    const int *ttab = s_tok + buf * kGmN;
-                    const float *wtab = s_wt + buf * kGmN;
+                    const int *ttab = s_tok + buf * TN;
+                    const float *wtab = s_wt + buf * TN;
                     if (a.y) {
                         // w * D of these 16 pairs -> this warp's staging buffer [pair][its 32
                         // rows] -> one 128-byte bulk reduction per pair into
@@ -645,7 +698,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
 }

@@ -90,7 +90,7 @@ constexpr int kInCtaRouteMaxT = 2;
 
 struct Layout {
     size_t ctrl, logits, idx, w, counts, offsets, perm_tok, perm_slot, inv, masks, prefix, chunk_count, chunk_base, units,
-        tiles, qx, sx,
+        tiles, tiles2, qx, sx,
         ex, xsum, ximg, qh, sh, eh, himg, total;
 };
 
@@ -103,7 +103,7 @@ Layout layout(long long T, long long H, long long I, long long E, long long k) {
         return o;
     };
     const long long P = T * k, W = (T + 31) / 32;
-    const long long max_tiles = (P + kTileN - 1) / kTileN + E;
+    const long long max_tiles = (P + kTileMin - 1) / kTileMin + E;
     L.ctrl = take(256);
     L.logits = take(T * E * 4);
     L.idx = take(P * 4);
@@ -120,15 +120,16 @@ Layout layout(long long T, long long H, long long I, long long E, long long k) {
     L.chunk_base = take(NC * E * 4);
     L.units = take(E * (long long)sizeof(UnitRec));
     L.tiles = take(max_tiles * (long long)sizeof(Tile));
+    L.tiles2 = take(max_tiles * (long long)sizeof(Tile));
     L.qx = take(T * H);
     L.sx = take(T * (H / 32) * 4);
     L.ex = take(P * 4);
     L.xsum = take(T * (H / 32) * 4);
-    L.ximg = take(2 * (P + kTileN) * H * 2);  // hi + lo operand image, 128 rows of slack
+    L.ximg = take(2 * (P + kTileMax) * H * 2);  // hi + lo operand image, kTileMax rows of slack
     L.qh = take(P * I);
     L.sh = take(P * (I / 32) * 4);
     L.eh = take(P * 4);
-    L.himg = take(2 * (P + kTileN) * I * 2);
+    L.himg = take(2 * (P + kTileMax) * I * 2);
     L.total = off;
     return L;
 }
@@ -432,7 +433,9 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     }
     if (T == 0) return cuda_check("init_y_kernel");
     plan_kernel<<<1, 1024, 0, s>>>(offsets, E, T, ctrl, mode == MOEQ_MODE_GEMV ? at<UnitRec>(ws, L.units) : nullptr,
-                                   perm_tok, perm_slot, y ? w : nullptr, k, at<Tile>(ws, L.tiles));
+                                   perm_tok, perm_slot, y ? w : nullptr, k, at<Tile>(ws, L.tiles),
+                                   bits == 2 ? GemmCfg<true, 2>::TILE_N : GemmCfg<true, 3>::TILE_N, at<Tile>(ws, L.tiles2),
+                                   bits == 2 ? GemmCfg<false, 2>::TILE_N : GemmCfg<false, 3>::TILE_N);
     if (int rc = cuda_check("plan_kernel")) return rc;
     if (mode == MOEQ_MODE_GEMV) {
         if (out_sorted) cudaMemsetAsync(out_sorted, 0, (size_t)P * H * sizeof(float), s);
@@ -474,7 +477,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     float *sh = sh_out ? sh_out : at<float>(ws, L.sh);
     int *eh = at<int>(ws, L.eh);
     __half *himg = at<__half>(ws, L.himg);
-    const long long img_rows = P + kTileN;  // a tile's rows may run up to 127 past P
+    const long long img_rows = P + kTileMax;  // a tile's rows may run up to kTileMax - 1 past P
     // x quantised per token, then its fp16 hi/lo rows written in sorted pair
     // order (pre-swizzled per tile) so that every GEMM tile reads one
     // contiguous run of B rows per K stage
@@ -483,7 +486,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     const unsigned split_blocks = (unsigned)std::min<long long>((P + 7) / 8, (long long)sm_count() * 16);
     split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, T, offsets, E, ximg, img_rows, ex);
     if (int rc = cuda_check("split_rows_kernel(x)")) return rc;
-    const long long max_tiles = (P + kTileN - 1) / kTileN + E;
+    const long long max_tiles = (P + kTileMin - 1) / kTileMin + E;
     GemmArgs g{};
     g.T = T;
     g.H = H;
@@ -495,7 +498,7 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
         g.scales[m] = wq->scales[m];
     }
     g.tiles = at<Tile>(ws, L.tiles);
-    g.ctrl = ctrl;
+    g.ntiles = ctrl + 2;
     g.perm_tok = perm_tok;
     g.perm_slot = perm_slot;
     g.w = w;
@@ -509,6 +512,8 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     split_rows_kernel<<<split_blocks, 256, 0, s>>>(qh, sh, I, nullptr, (int)P, (int)P, offsets, E, himg, img_rows, eh);
     if ((rc = cuda_check("split_rows_kernel(h)"))) return rc;
     g.bimg = himg;
+    g.tiles = at<Tile>(ws, L.tiles2);
+    g.ntiles = ctrl + kCtrlTiles2;
     g.brow_exp = eh;
     g.y = y;
     g.out_sorted = out_sorted;

@@ -155,9 +155,11 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const int32_t *__r
 
 // Work plan from offsets: the number of experts with at least one pair and
 // their UnitRec records (for the decode expert kernel; units may be NULL), and
-// the list of (expert, first sorted position, rows) tiles of up to kTileN
-// pairs (for the tensor-core kernels).
-constexpr int kTileN = 128;
+// two lists of (expert, first sorted position, rows) tiles, of up to tile_n
+// and up to tile_n2 pairs (for the two tensor-core kernels; multiples of 16 in
+// [kTileMin, kTileMax]), counted in ctrl[2] and ctrl[kCtrlTiles2].
+constexpr int kTileMin = 64, kTileMax = 128;
+constexpr int kCtrlTiles2 = 8;
 
 struct Tile {
     int e, p0, n, pad;
@@ -166,9 +168,11 @@ struct Tile {
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ offsets, int E, int T, int *ctrl,
                                                     UnitRec *units, const int32_t *__restrict__ perm_tok,
                                                     const int32_t *__restrict__ perm_slot,
-                                                    const float *__restrict__ w, int k, Tile *tiles) {
+                                                    const float *__restrict__ w, int k, Tile *tiles, int tile_n,
+                                                    Tile *tiles2, int tile_n2) {
     __shared__ int s_act[kMaxE];
     __shared__ int s_til[kMaxE];
+    __shared__ int s_til2[kMaxE];
     __shared__ int s_scan[33];
     __shared__ int s_bad;
     const int tid = threadIdx.x;
@@ -179,7 +183,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         const int c = offsets[e + 1] - offsets[e];
         if (c < 0) s_bad = 1;
         s_act[e] = c > 0;
-        s_til[e] = (c + kTileN - 1) / kTileN;
+        s_til[e] = (c + tile_n - 1) / tile_n;
+        s_til2[e] = (c + tile_n2 - 1) / tile_n2;
     }
     __syncthreads();
     if (s_bad) {  // offsets that are not a prefix sum over [0, T*k]: no work at all
@@ -187,11 +192,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
             set_status(MOEQ_STATUS_BAD_INDEX);
             ctrl[1] = 0;
             ctrl[2] = 0;
+            ctrl[kCtrlTiles2] = 0;
         }
         return;
     }
     const int n_active = block_exclusive_scan(s_act, E, s_scan);
     const int n_tiles = block_exclusive_scan(s_til, E, s_scan);
+    const int n_tiles2 = block_exclusive_scan(s_til2, E, s_scan);
     for (int e = tid; e < E; e += blockDim.x) {
         const int o = offsets[e], c = offsets[e + 1] - o;
         if (c > 0 && units) {
@@ -211,18 +218,27 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
                 r->w[i] = wv;
             }
         }
-        for (int i = 0; i * kTileN < c; ++i) {
+        for (int i = 0; i * tile_n < c; ++i) {
             Tile tl;
             tl.e = e;
-            tl.p0 = o + i * kTileN;
-            tl.n = min(kTileN, c - i * kTileN);
+            tl.p0 = o + i * tile_n;
+            tl.n = min(tile_n, c - i * tile_n);
             tl.pad = 0;
             tiles[s_til[e] + i] = tl;
+        }
+        for (int i = 0; i * tile_n2 < c; ++i) {
+            Tile tl;
+            tl.e = e;
+            tl.p0 = o + i * tile_n2;
+            tl.n = min(tile_n2, c - i * tile_n2);
+            tl.pad = 0;
+            tiles2[s_til2[e] + i] = tl;
         }
     }
     if (tid == 0) {
         ctrl[1] = n_active;
         ctrl[2] = n_tiles;
+        ctrl[kCtrlTiles2] = n_tiles2;
     }
 }
 

@@ -84,11 +84,11 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict
 // contiguous run of rows that lands in shared memory already in the 128-byte
 // swizzled K-major form the MMA descriptors expect:
 //   img[st][half][row][64]  (st = K stage of 64 values, half 0 = hi, 1 = lo,
-//                            rows = img_rows >= rows + 128 per (st, half))
+//                            rows = img_rows >= rows + kTileMax per (st, half))
 // and the 16-byte chunk c of a 128-byte stage row is stored at chunk
 // c ^ ((r - t0) & 7), t0 = the first row of r's tile.  Tiles start at every
-// 128th position of each expert's segment [offsets[e], offsets[e+1]), so the
-// phase is (r - offsets[e]) & 7.  One warp per output row, one 16-byte chunk
+// tile_n-th position of each expert's segment [offsets[e], offsets[e+1]),
+// tile_n a multiple of 16, so the phase is (r - offsets[e]) & 7.  One warp per output row, one 16-byte chunk
 // of each half per lane per step.
 __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restrict__ q, const float *__restrict__ s,
                                                          int n, const int32_t *__restrict__ row_map, int rows,
