@@ -179,12 +179,16 @@ struct GemmCfg {
     static constexpr int NA = GATEUP ? 2 : 1;  // weight matrices per work item (gate + up, or down)
     static constexpr int BPB = 4 * BITS;
     static constexpr int NAT = BITS == 3 ? 2 : 1;  // weight panels per matrix: hi (, lo)
-    // tokens per tile (MMA N): TMEM holds two accumulator buffers of NA x TILE_N
-    // columns and PSTAGES weight panels of NAT x NA x 32 columns (K = 64 fp16)
-    static constexpr int TILE_N = GATEUP ? (BITS == 2 ? 96 : 64) : 128;
+    // tokens per tile (MMA N): TMEM holds NBUF accumulator buffers of NA x TILE_N
+    // columns and PSTAGES weight panels of NAT x NA x 32 columns (K = 64 fp16).
+    // 3-bit gate/up needs 128 columns per panel stage, so it keeps 128-token
+    // tiles (half the MMAs of 64-token ones) with one accumulator buffer: its
+    // epilogue then does not overlap the next item's MMAs
+    static constexpr int NBUF = (GATEUP && BITS == 3) ? 1 : 2;
+    static constexpr int TILE_N = (GATEUP && BITS == 2) ? 96 : 128;
     static constexpr int ACC_COLS = NA * TILE_N;           // one accumulator buffer (fp32 columns)
     static constexpr int A_COLS = NAT * NA * (kGmK / 2);   // one stage of weight panels
-    static constexpr int A_BASE = 2 * ACC_COLS;            // first panel column
+    static constexpr int A_BASE = NBUF * ACC_COLS;         // first panel column
 #if defined(MOEQ_GEMM_PSTAGES)
     static constexpr int PSTAGES = MOEQ_GEMM_PSTAGES;
 #else
@@ -194,7 +198,7 @@ struct GemmCfg {
 #if defined(MOEQ_GEMM_STAGES)
     static constexpr int STAGES = MOEQ_GEMM_STAGES;
 #else
-    static constexpr int STAGES = GATEUP ? 6 : 5;
+    static constexpr int STAGES = GATEUP ? (BITS == 2 ? 6 : 4) : 5;
 #endif
     static constexpr int RSTAGES = 6;                    // raw-code ring (runs further ahead)
     static constexpr int B_BYTES = TILE_N * kGmK * 2;    // fp16 activation tile (hi or lo)
@@ -272,6 +276,7 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
 //              TMEM lane quadrant w % 4
 //   warps 6-9  epilogue on the other accumulator buffer (TMEM lane quadrant
 //              = warp % 4), so item i's epilogue overlaps item i+1's MMAs
+//              (with one buffer, 3-bit gate/up, the MMAs wait for it)
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag,
 // every role leaves its loop, copies and MMAs are drained and TMEM is freed.
 template <bool GATEUP, int BITS>
@@ -443,8 +448,8 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                 const int nround = (tl.n + 15) & ~15;
                 const bool cat = nround <= TN / 2;
                 const uint32_t idesc = f16_idesc(kGmM, cat ? 2 * nround : nround);
-                const int buf = j & 1;
-                if (!MOEQ_GW(3, mbar_wait(smem_u32(&acc_empty[buf]), ((j >> 1) & 1) ^ 1, abort_flag, wl))) break;
+                const int buf = j % C::NBUF;
+                if (!MOEQ_GW(3, mbar_wait(smem_u32(&acc_empty[buf]), ((j / C::NBUF) & 1) ^ 1, abort_flag, wl))) break;
                 MOEQ_TL_TAG(TLK, 0, ((unsigned)j << 8) | blockIdx.x);
                 tc_fence_after();
                 const uint32_t acc0 = tmem + (uint32_t)(buf * C::ACC_COLS);
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
         for (int j = 0; j < nq; ++j) {
             const Tile tl = item_tile(j);
             const int m0 = item_m0(j);
-            const int buf = j & 1, p0 = tl.p0, nval = tl.n, nround = (nval + 15) & ~15;
+            const int buf = j % C::NBUF, p0 = tl.p0, nval = tl.n, nround = (nval + 15) & ~15;
             if (et < TN) {
                 const int p = p0 + min(et, nval - 1);
                 int t = a.perm_tok[p];
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             named_sync(1, 128);
             if (dead) continue;
             // one decision for all four epilogue warps (they meet at named barriers below)
-            if (named_sync_or(3, 128, !MOEQ_GW(10, mbar_wait(smem_u32(&acc_full[buf]), (j >> 1) & 1, abort_flag, wl)))) {
+            if (named_sync_or(3, 128, !MOEQ_GW(10, mbar_wait(smem_u32(&acc_full[buf]), (j / C::NBUF) & 1, abort_flag, wl)))) {
                 dead = true;
                 continue;
             }
