@@ -183,8 +183,9 @@ struct GemmCfg {
     // columns and PSTAGES weight panels of NAT x NA x 32 columns (K = 64 fp16).
     // 3-bit gate/up needs 128 columns per panel stage, so it keeps 128-token
     // tiles (half the MMAs of 64-token ones) with one accumulator buffer: its
-    // epilogue then does not overlap the next item's MMAs
-    static constexpr int NBUF = (GATEUP && BITS == 3) ? 1 : 2;
+    // epilogue then does not overlap the next item's MMAs.  Down (8 stages per
+    // item, a comparatively long epilogue) has room for three
+    static constexpr int NBUF = GATEUP ? (BITS == 3 ? 1 : 2) : 3;
     static constexpr int TILE_N = (GATEUP && BITS == 2) ? 96 : 128;
     static constexpr int ACC_COLS = NA * TILE_N;           // one accumulator buffer (fp32 columns)
     static constexpr int A_COLS = NAT * NA * (kGmK / 2);   // one stage of weight panels
@@ -206,8 +207,8 @@ struct GemmCfg {
     static constexpr int RAW_CODES = NA * 2 * kGmM * BPB;  // two K-blocks per stage
     static constexpr int RAW_SCALES = NA * 2 * kGmM * 2;
     static constexpr int RAW_BYTES = RAW_CODES + RAW_SCALES;
-    static constexpr int NUM_BARS = 2 * RSTAGES + 2 * STAGES + 2 * PSTAGES + 5;
-    static constexpr int MISC_BYTES = 8 * NUM_BARS + 16 + 3 * 2 * TILE_N * 4;
+    static constexpr int NUM_BARS = 2 * RSTAGES + 2 * STAGES + 2 * PSTAGES + 2 * NBUF + 1;
+    static constexpr int MISC_BYTES = 8 * NUM_BARS + 16 + 3 * NBUF * TILE_N * 4;
     // down: per epilogue warp two staging buffers of 16 tokens x its 32 rows of
     // w * D (fp32) that it adds into y with bulk reductions
     static constexpr int STAGE_BYTES = GATEUP ? 0 : 2 * 16 * kGmM * 4;
@@ -299,13 +300,13 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
     uint64_t *raw_full = bars, *raw_empty = bars + R;
     uint64_t *b_full = bars + 2 * R, *b_empty = b_full + S;
     uint64_t *a_full = b_empty + S, *a_empty = a_full + PS;
-    uint64_t *acc_full = a_empty + PS, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+    uint64_t *acc_full = a_empty + PS, *acc_empty = acc_full + C::NBUF, *drain = acc_empty + C::NBUF;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *s_tok = reinterpret_cast<int *>(tmem_slot + 4);  // [2][TN] per accumulator buffer
-    int *s_exp = s_tok + 2 * TN;
-    float *s_wt = reinterpret_cast<float *>(s_exp + 2 * TN);
-    float *s_stage = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_wt + 2 * TN) + 127) & ~(uintptr_t)127);
+    int *s_tok = reinterpret_cast<int *>(tmem_slot + 4);  // [NBUF][TN] per accumulator buffer
+    int *s_exp = s_tok + C::NBUF * TN;
+    float *s_wt = reinterpret_cast<float *>(s_exp + C::NBUF * TN);
+    float *s_stage = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_wt + C::NBUF * TN) + 127) & ~(uintptr_t)127);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t wl = wait_limit();
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             mbar_init(smem_u32(&a_full[i]), C::UNPACK);
             mbar_init(smem_u32(&a_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NBUF; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), 128);
         }
