@@ -279,7 +279,11 @@ __device__ __forceinline__ bool gemv_unit(const GemvArgs &a, int u, int *tok, fl
     return true;
 }
 
-template <int BITS, int PER>
+// MAXNT: the most tokens a pass holds (a.tc <= MAXNT).  The single-token
+// instantiation carries one block-dot loop instead of eight; B = 1 decode
+// launches run it, and its smaller code takes fewer instruction-cache misses
+// in CTAs that each run the body once.
+template <int BITS, int PER, int MAXNT>
 __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ GemvArgs a) {
     constexpr int BPB = 4 * BITS;
     constexpr int OFF = 1 << (BITS - 1);
@@ -451,15 +455,19 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
 #define MOEQ_GU(NT_)                                                                                             \
     gu_accumulate<BITS, NT_>(acc, gu_codes, gu_scales, xpack, xs, xsum, xrow, m, q4, a.kc, kb0, nkb, KBH, lane); \
     break
-            switch (nt) {
-                case 1: MOEQ_GU(1);
-                case 2: MOEQ_GU(2);
-                case 3: MOEQ_GU(3);
-                case 4: MOEQ_GU(4);
-                case 5: MOEQ_GU(5);
-                case 6: MOEQ_GU(6);
-                case 7: MOEQ_GU(7);
-                default: MOEQ_GU(8);
+            if (MAXNT == 1) {
+                gu_accumulate<BITS, 1>(acc, gu_codes, gu_scales, xpack, xs, xsum, xrow, m, q4, a.kc, kb0, nkb, KBH, lane);
+            } else {
+                switch (nt) {
+                    case 1: MOEQ_GU(1);
+                    case 2: MOEQ_GU(2);
+                    case 3: MOEQ_GU(3);
+                    case 4: MOEQ_GU(4);
+                    case 5: MOEQ_GU(5);
+                    case 6: MOEQ_GU(6);
+                    case 7: MOEQ_GU(7);
+                    default: MOEQ_GU(8);
+                }
             }
 #undef MOEQ_GU
         }

@@ -326,12 +326,12 @@ int tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint64_t e
     return MOEQ_OK;
 }
 
-template <int BITS, int PER>
+template <int BITS, int PER, int MAXNT>
 int launch_gemv(GemvArgs g, int T, int k, int E, cudaStream_t s) {
     const int cap = max_smem_optin();
     g.kc = std::min(g.H / 32, kGvMaxKB);
     g.rc = std::min(g.H, kGvMaxRows);
-    g.tc = kGvTok;
+    g.tc = MAXNT;
     auto need = [&]() { return (int)gemv_smem(g.H, BITS, g.kc, g.rc, g.tc).total; };
     while (need() > cap && g.tc > 1) g.tc /= 2;
     while (need() > cap && g.kc > 4) g.kc = (g.kc + 1) / 2;
@@ -348,13 +348,13 @@ int launch_gemv(GemvArgs g, int T, int k, int E, cudaStream_t s) {
                              (uint32_t)g.kc, CU_TENSOR_MAP_SWIZZLE_NONE))
             return rc;
     }
-    cudaError_t e = cudaFuncSetAttribute(ffn_gemv_kernel<BITS, PER>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(ffn_gemv_kernel<BITS, PER, MAXNT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "gemv smem attribute: %s", cudaGetErrorString(e));
     const long long units = std::min<long long>((long long)T * k, E);
     const long long blocks = units * (g.I / 32);
     if (blocks == 0) return MOEQ_OK;
     trace_begin(s);
-    e = launch_pdl(ffn_gemv_kernel<BITS, PER>, (unsigned)blocks, 256, (size_t)smem, s, g);
+    e = launch_pdl(ffn_gemv_kernel<BITS, PER, MAXNT>, (unsigned)blocks, 256, (size_t)smem, s, g);
     trace_end(s);
     if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "ffn_gemv_kernel: %s", cudaGetErrorString(e));
     return cuda_check("ffn_gemv_kernel");
@@ -362,7 +362,10 @@ int launch_gemv(GemvArgs g, int T, int k, int E, cudaStream_t s) {
 
 int gemv_dispatch(const GemvArgs &g, int bits, int T, int k, int E, cudaStream_t s) {
     const int per = (E + 31) / 32;
-#define MOEQ_GEMV(P_) return bits == 2 ? launch_gemv<2, P_>(g, T, k, E, s) : launch_gemv<3, P_>(g, T, k, E, s)
+    // one token: the single-token kernel (every unit then holds one pair)
+#define MOEQ_GEMV(P_)                                                                              \
+    return T == 1 ? (bits == 2 ? launch_gemv<2, P_, 1>(g, T, k, E, s) : launch_gemv<3, P_, 1>(g, T, k, E, s)) \
+                  : (bits == 2 ? launch_gemv<2, P_, kGvTok>(g, T, k, E, s) : launch_gemv<3, P_, kGvTok>(g, T, k, E, s))
     if (per <= 1) MOEQ_GEMV(1);
     if (per <= 2) MOEQ_GEMV(2);
     if (per <= 4) MOEQ_GEMV(4);
