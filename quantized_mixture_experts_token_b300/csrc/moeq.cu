@@ -229,18 +229,27 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, si
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int PER>
-int launch_route_gemv(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
-                      const DecodeTail &tail, cudaStream_t s) {
+template <int PER, int MAXT>
+int launch_route_gemv_t(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
+                        const DecodeTail &tail, cudaStream_t s) {
     const size_t smem = route_smem(H, E).total;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(route_gemv_kernel<PER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(route_gemv_kernel<PER, MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "route smem attribute: %s", cudaGetErrorString(e));
     }
     const unsigned blocks = (unsigned)((E + kRouteRows - 1) / kRouteRows);
-    cudaError_t e = launch_pdl(route_gemv_kernel<PER>, blocks, 256, smem, s, x, T, H, Wr, bias, E, logits, tail);
+    cudaError_t e = launch_pdl(route_gemv_kernel<PER, MAXT>, blocks, 256, smem, s, x, T, H, Wr, bias, E, logits, tail);
     if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "route_gemv_kernel: %s", cudaGetErrorString(e));
     return MOEQ_OK;
+}
+
+// One token (and no routing tail): the single-token router kernel.
+template <int PER>
+int launch_route_gemv(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,
+                      const DecodeTail &tail, cudaStream_t s) {
+    if (T == 1 && tail.mode < 2) return launch_route_gemv_t<PER, 1>(x, T, H, Wr, bias, E, logits, tail, s);
+    return launch_route_gemv_t<PER, kRouteTok>(x, T, H, Wr, bias, E, logits, tail, s);
 }
 
 int route_gemv_dispatch(const float *x, int T, int H, const float *Wr, const float *bias, int E, float *logits,

@@ -211,8 +211,8 @@ __host__ __device__ inline RouteSmem route_smem(int H, int E) {
 
 // Router partial dot products of this warp's columns [h_begin, h_end) of one
 // shared-memory chunk for up to NT tokens (nt <= NT active).
-template <int NT>
-__device__ __forceinline__ void route_accumulate(float (&acc)[kRouteRows][kRouteTok], const float *wr, int hc, int nr,
+template <int NT, int AT>
+__device__ __forceinline__ void route_accumulate(float (&acc)[kRouteRows][AT], const float *wr, int hc, int nr,
                                                  const float *x, int H, int t0, int c0, int h_begin, int h_end,
                                                  int lane, int nt) {
     for (int h = h_begin + 4 * lane; h < h_end; h += 128) {
@@ -232,8 +232,8 @@ __device__ __forceinline__ void route_accumulate(float (&acc)[kRouteRows][kRoute
     }
 }
 
-template <int NT>
-__device__ __forceinline__ void route_reduce(const float (&acc)[kRouteRows][kRouteTok], float (*part)[kRouteRows][kRouteTok],
+template <int NT, int AT>
+__device__ __forceinline__ void route_reduce(const float (&acc)[kRouteRows][AT], float (*part)[kRouteRows][kRouteTok],
                                              int warp, int lane) {
 #pragma unroll
     for (int r = 0; r < kRouteRows; ++r)
@@ -244,7 +244,10 @@ __device__ __forceinline__ void route_reduce(const float (&acc)[kRouteRows][kRou
         }
 }
 
-template <int PER>
+// MAXT: the most tokens of a call (1 or kRouteTok).  The single-token
+// instantiation keeps one accumulator per router row and none of the routing
+// tail: B = 1 decode launches run it, with less code to fetch per CTA.
+template <int PER, int MAXT>
 __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict__ x, int T, int H,
                                                          const float *__restrict__ Wr,
                                                          const float *__restrict__ bias, int E,
@@ -291,11 +294,11 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
     uint32_t ph = 0;
     for (int t0 = 0; t0 < T && !failed; t0 += kRouteTok) {
         const int nt = min(kRouteTok, T - t0);
-        float acc[kRouteRows][kRouteTok];
+        float acc[kRouteRows][MAXT];
 #pragma unroll
         for (int r = 0; r < kRouteRows; ++r)
 #pragma unroll
-            for (int t = 0; t < kRouteTok; ++t) acc[r][t] = 0.f;
+            for (int t = 0; t < MAXT; ++t) acc[r][t] = 0.f;
         for (int c = 0; c < nhc; ++c) {
             if (loaded != c) {  // only when H > kRouteHC
                 __syncthreads();
@@ -316,18 +319,18 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
             const int c0 = c * hc, w = min(hc, H - c0);
             const int ws = w / 8;  // multiple of 16
             const int hb = warp * ws, he = hb + ws;
-            if (nt == 1) route_accumulate<1>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
-            else if (nt == 2) route_accumulate<2>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
-            else if (nt <= 4) route_accumulate<4>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
-            else if (nt <= 8) route_accumulate<8>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
-            else route_accumulate<16>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
+            if (MAXT == 1 || nt == 1) route_accumulate<1, MAXT>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
+            else if (nt == 2) route_accumulate<2, MAXT>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
+            else if (nt <= 4) route_accumulate<4, MAXT>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
+            else if (nt <= 8) route_accumulate<8, MAXT>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
+            else route_accumulate<16, MAXT>(acc, wr, hc, nr, x, H, t0, c0, hb, he, lane, nt);
         }
         if (failed) break;
-        if (nt == 1) route_reduce<1>(acc, part, warp, lane);
-        else if (nt == 2) route_reduce<2>(acc, part, warp, lane);
-        else if (nt <= 4) route_reduce<4>(acc, part, warp, lane);
-        else if (nt <= 8) route_reduce<8>(acc, part, warp, lane);
-        else route_reduce<16>(acc, part, warp, lane);
+        if (MAXT == 1 || nt == 1) route_reduce<1, MAXT>(acc, part, warp, lane);
+        else if (nt == 2) route_reduce<2, MAXT>(acc, part, warp, lane);
+        else if (nt <= 4) route_reduce<4, MAXT>(acc, part, warp, lane);
+        else if (nt <= 8) route_reduce<8, MAXT>(acc, part, warp, lane);
+        else route_reduce<16, MAXT>(acc, part, warp, lane);
         __syncthreads();
         MOEQ_TL(1, 5);
         if (tid < kRouteRows * kRouteTok) {
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
 
     if (failed && tid == 0 && !ready) mbar_drain(bar, ph & 1, &s_abort);  // the copy in flight lands first
     MOEQ_TL(1, 3);
-    if (tail.mode < 2) return;
+    if (MAXT == 1 || tail.mode < 2) return;  // the routing tail serves T >= 3 only
 
     // ---- the last CTA to finish ranks every token and groups the pairs by expert.
     // The barrier orders this CTA's logit and quantisation writes before thread
