@@ -155,6 +155,32 @@ def test_route_topk_full(full, full_skew, cuda_lib, T):
         _check_routing(case, x, idx, w)
 
 
+@pytest.mark.parametrize("n_tied", [512, 40])
+@pytest.mark.parametrize("T,fused", [(1, True), (2, True), (8, False)])
+def test_routing_heavy_ties_full(full, cuda_lib, n_tied, T, fused):
+    """Exact ties among more than 32 logits at the top take the warp top-k's
+    rare paths (more candidates than lanes).  x = 0 gives logits equal to the
+    bias: all 512 tied, or the first 40 at +1 and the rest at 0.  Ties go to the
+    lower expert index; the oracle's stable sort says the same."""
+    shape = full.shape
+    x = torch.zeros(T, shape.H)
+    bias = torch.zeros(shape.E)
+    if n_tied < shape.E:
+        bias[:n_tied] = 1.0
+    L = oracle.router_logits(x.numpy(), full.dev.Wr.cpu().numpy(), bias.numpy())
+    ref_idx, ref_w = oracle.topk_softmax(L, shape.k)
+    ws = _ws(cuda_lib, T, shape)
+    if fused:  # through the fused decode tail (in-CTA ranking for T <= 2)
+        _, idx, w = cuda_lib.layer_forward(x.to(_dev()), full.W, full.dev.Wr, bias.to(_dev()), shape.k, ws,
+                                           want_routing=True)
+    else:
+        idx, w = cuda_lib.route_topk(x.to(_dev()), full.dev.Wr, bias.to(_dev()), shape.k, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.allclose(w.cpu().numpy(), ref_w, rtol=1e-6, atol=0)
+    assert cuda_lib.device_status() == 0
+
+
 # ------------------------------------------------------------- permutation
 
 
