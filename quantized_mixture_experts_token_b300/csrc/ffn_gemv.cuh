@@ -167,8 +167,8 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
 // Gate/up partial sums over this warp's K-blocks (kl = q4, q4+4, ...) of one
 // shared-memory chunk for NT tokens.  NT is a compile-time count so that no
 // issue slot is spent on absent tokens.
-template <int BITS, int NT>
-__device__ __forceinline__ void gu_accumulate(float (&acc)[kGvTok], const unsigned char *gu_codes,
+template <int BITS, int NT, int AT>
+__device__ __forceinline__ void gu_accumulate(float (&acc)[AT], const unsigned char *gu_codes,
                                               const uint16_t *gu_scales, const int4 *xpack, const float *xs,
                                               const int *xsum, const int *xrow, int m, int q4, int kc, int kb0,
                                               int nkb, int KBH, int lane) {
@@ -431,9 +431,9 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
         }
         // 2. gate / up: warp (m, q) sums K-blocks q, q+4, ... of matrix m
         const int m = warp >> 2, q4 = warp & 3;
-        float acc[kGvTok];
+        float acc[MAXNT];
 #pragma unroll
-        for (int s = 0; s < kGvTok; ++s) acc[s] = 0.f;
+        for (int s = 0; s < MAXNT; ++s) acc[s] = 0.f;
         for (int gc = 0; gc < ngc; ++gc) {
             if (gu_chunk != gc) {  // only when the slice is streamed in pieces
                 __syncthreads();
@@ -453,10 +453,10 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
             }
             const int kb0 = gc * a.kc, nkb = min(a.kc, KBH - kb0);
 #define MOEQ_GU(NT_)                                                                                             \
-    gu_accumulate<BITS, NT_>(acc, gu_codes, gu_scales, xpack, xs, xsum, xrow, m, q4, a.kc, kb0, nkb, KBH, lane); \
+    gu_accumulate<BITS, (NT_ < MAXNT ? NT_ : MAXNT), MAXNT>(acc, gu_codes, gu_scales, xpack, xs, xsum, xrow, m, q4, a.kc, kb0, nkb, KBH, lane); \
     break
             if (MAXNT == 1) {
-                gu_accumulate<BITS, 1>(acc, gu_codes, gu_scales, xpack, xs, xsum, xrow, m, q4, a.kc, kb0, nkb, KBH, lane);
+                gu_accumulate<BITS, 1, MAXNT>(acc, gu_codes, gu_scales, xpack, xs, xsum, xrow, m, q4, a.kc, kb0, nkb, KBH, lane);
             } else {
                 switch (nt) {
                     case 1: MOEQ_GU(1);
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(256) ffn_gemv_kernel(const __grid_constant__ G
         }
         if (failed) break;
 #pragma unroll
-        for (int s = 0; s < kGvTok; ++s) part[((m * 4 + q4) * kGvTok + s) * 32 + lane] = acc[s];
+        for (int s = 0; s < MAXNT; ++s) part[((m * 4 + q4) * kGvTok + s) * 32 + lane] = acc[s];
         __syncthreads();
         MOEQ_TL(2, 5);
         // 3. SwiGLU and re-quantisation of this I-block, one warp per token
