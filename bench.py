@@ -55,8 +55,8 @@ SWEEP_T = (8, 16, 32, 64, 128, 256, 512, 1024)  # token counts of the GEMV / gro
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # current kernel versions from one ncu --set full capture (profiles/), with
 # its source; set to None when a kernel changes until it is captured again
-DECODE_LAYER_TRAFFIC = dict(bytes=4.269056e6 + 9.927936e6,
-                            source=("ncu: route_gemv_kernel 4.27 MB + ffn_gemv_kernel 9.93 MB, one B=1 layer "
+DECODE_LAYER_TRAFFIC = dict(bytes=4.220416e6 + 9.925376e6,
+                            source=("ncu: route_gemv_kernel 4.22 MB + ffn_gemv_kernel 9.93 MB, one B=1 layer "
                                     "(profiles/route_gemv_decode_T1.md, ffn_gemv_decode_T1.md)"))
 GEMM_GU_TRAFFIC = dict(bytes=691.945728e6 + 20.323328e6,
                        source="ncu: ffn_gemm_kernel<1,2> 691.9 MB read + 20.3 MB written (profiles/ffn_gemm_gateup_prefill_4k.md)")
