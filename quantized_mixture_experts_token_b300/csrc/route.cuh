@@ -446,80 +446,4 @@ __global__ void __launch_bounds__(256) route_gemv_kernel(const float *__restrict
     MOEQ_TL(1, 4);
 }
 
-// ------------------------------------------------- router logits, large T
-
-// Plain SIMT SGEMM  L[T,E] = x[T,H] Wr[E,H]^T + b: 128x64 tile per CTA, 256
-// threads with 8x4 outputs each, K-slabs of 16 staged transposed in shared
-// memory.
-constexpr int kSgBM = 128, kSgBN = 64, kSgBK = 16;
-
-__global__ void __launch_bounds__(256) route_sgemm_kernel(const float *__restrict__ x, int T, int H,
-                                                          const float *__restrict__ Wr,
-                                                          const float *__restrict__ bias, int E,
-                                                          float *__restrict__ logits) {
-    __shared__ float As[2][kSgBK][kSgBM + 4];
-    __shared__ float Bs[2][kSgBK][kSgBN + 4];
-    const int tid = threadIdx.x;
-    const int m0 = blockIdx.y * kSgBM, n0 = blockIdx.x * kSgBN;
-    const int tx = tid % 16, ty = tid / 16;  // 16 x 16 threads; thread owns rows ty*8.., cols tx*4..
-    float acc[8][4] = {};
-    // loaders: A tile 128x16 = 512 float4 (2 per thread), B tile 64x16 = 256 float4 (1 per thread)
-    auto load = [&](int buf, int k0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            int f = tid + 256 * i;
-            int r = f / 4, c = (f % 4) * 4;
-            int gr = m0 + r;
-            float4 v = gr < T ? __ldg(reinterpret_cast<const float4 *>(x + (size_t)gr * H + k0 + c))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            As[buf][c + 0][r] = v.x;
-            As[buf][c + 1][r] = v.y;
-            As[buf][c + 2][r] = v.z;
-            As[buf][c + 3][r] = v.w;
-        }
-        {
-            int r = tid / 4, c = (tid % 4) * 4;
-            int gr = n0 + r;
-            float4 v = gr < E ? __ldg(reinterpret_cast<const float4 *>(Wr + (size_t)gr * H + k0 + c))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            Bs[buf][c + 0][r] = v.x;
-            Bs[buf][c + 1][r] = v.y;
-            Bs[buf][c + 2][r] = v.z;
-            Bs[buf][c + 3][r] = v.w;
-        }
-    };
-    load(0, 0);
-    __syncthreads();
-    const int nk = H / kSgBK;
-    for (int kt = 0; kt < nk; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < nk) load(buf ^ 1, (kt + 1) * kSgBK);
-#pragma unroll
-        for (int kk = 0; kk < kSgBK; ++kk) {
-            float a[8], b[4];
-            float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][ty * 8]);
-            float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][ty * 8 + 4]);
-            float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][tx * 4]);
-            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-            a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-            b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int r = m0 + ty * 8 + i;
-        if (r >= T) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int c = n0 + tx * 4 + j;
-            if (c < E) logits[(size_t)r * E + c] = acc[i][j] + (bias ? bias[c] : 0.f);
-        }
-    }
-}
-
 }  // namespace moeq
