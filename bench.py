@@ -385,6 +385,30 @@ def prefill_chunk(gpu, pre_layer, preW, args, rank):
     pe = aggregate(Tp * psteps, gpu.timed(e2e, psteps, args.warmup), gpu.world)
     tf32_peak = pk["bf16"] / 2.0  # tf32 dense rate is half the bf16 rate (nominal 1.1 vs 2.25 PFLOP/s)
     s8 = s8_peak_tops()
+
+    # the same chunk with both expert GEMMs on the warp-level int8 path
+    # (exact block products scaled in registers): the comparison point
+    def call_s8():
+        moeq.layer_forward(xp, preW, pre_layer.Wr, pre_layer.bias, K_TOP, wsp, y=yp, mode=moeq.MODE_GEMM_S8)
+
+    g8 = gpu.graph(call_s8)
+    ev8 = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    moeq.trace_events(ev8)
+    g8_tr = gpu.graph(call_s8)
+    moeq.trace_events(None)
+    pre8 = aggregate(Tp * psteps, gpu.timed(g8.replay, psteps, args.warmup), gpu.world)
+    for _ in range(3):
+        g8_tr.replay()
+    torch.cuda.synchronize()
+    gu8_s, dn8_s = (ev8[2 * i].elapsed_time(ev8[2 * i + 1]) / 1e3 for i in (1, 2))
+    s8_path = dict(
+        kernel="ffn_mma8_kernel: mma.sync m16n8k32 s8, every 32-block product an exact integer dot scaled in registers",
+        value=pre8["value"], unit="tokens/s", ms_per_chunk=1e3 * pre8["seconds"] / psteps,
+        gateup=dict(launch_us=gu8_s * 1e6, achieved_tops=gu_flop / gu8_s / 1e12,
+                    frac_of_s8=(gu_flop / gu8_s / 1e12 / s8) if s8 else None),
+        down=dict(launch_us=dn8_s * 1e6, achieved_tops=dn_flop / dn8_s / 1e12,
+                  frac_of_s8=(dn_flop / dn8_s / 1e12 / s8) if s8 else None),
+        s8_peak_tops=s8)
     return dict(
         value=pre["value"], unit="tokens/s", ms_per_chunk=1e3 * pre["seconds"] / psteps,
         workload="prefill: 4,096-token chunk through one 2048/512/512 top-10 2-bit layer, Zipf(1.1)-skewed router",
@@ -402,7 +426,8 @@ def prefill_chunk(gpu, pre_layer, preW, args, rank):
                       router=dict(achieved=rt_flop / rt_s / 1e12, frac_of_tf32=rt_flop / rt_s / 1e12 / tf32_peak,
                                   launch_us=rt_s * 1e6, flop_per_launch=rt_flop, kernel="route_tc_kernel (3xTF32)",
                                   peak_source="tf32 = measured bf16 / 2")),
-        e2e=dict(value=pe["value"], unit="tokens/s", h2d_bytes_per_step=Tp * H * 4, d2h_bytes_per_step=Tp * H * 4))
+        e2e=dict(value=pe["value"], unit="tokens/s", h2d_bytes_per_step=Tp * H * 4, d2h_bytes_per_step=Tp * H * 4),
+        s8_path=s8_path)
 
 
 def stack_prompt(gpu, layers, Ws, args, rank):

@@ -69,8 +69,14 @@ extern "C" {
 #define MOEQ_MODE_AUTO 0 /* GEMV for T <= 512 (faster there on B300), grouped GEMM otherwise */
 #define MOEQ_MODE_GEMV 1 /* per-expert split GEMV with fused SwiGLU/down/combine */
 #define MOEQ_MODE_GEMM 2 /* grouped tcgen05 tensor-core GEMMs */
+/* Grouped GEMMs on the warp-level int8 tensor path (mma.sync s8), every
+ * 32-block product an exact integer dot scaled in registers: the int8 MMAs of
+ * the pages' fused prompt-expert kernels ("Strata - the details", "Speed
+ * (measured)", 0.1.36).  A comparison path, slower than MOEQ_MODE_GEMM on
+ * B300; MOEQ_MODE_AUTO never selects it. */
+#define MOEQ_MODE_GEMM_S8 3
 
-/* Supported shapes: H and I multiples of 128, 32 <= H <= 16384,
+/* Supported shapes: H and I multiples of 128, 128 <= H <= 16384,
  * 128 <= I <= 4096, 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0. */
 
 typedef struct moe_qweights {

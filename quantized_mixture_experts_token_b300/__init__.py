@@ -19,7 +19,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmoeq.so")
 
-MODE_AUTO, MODE_GEMV, MODE_GEMM = 0, 1, 2
+MODE_AUTO, MODE_GEMV, MODE_GEMM, MODE_GEMM_S8 = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT, STATUS_BAD_INDEX = 0x1, 0x2
 
 # Function names of the C ABI (include/moeq.h).

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "ffn_gemm.cuh"
 #include "ffn_gemv.cuh"
+#include "ffn_mma8.cuh"
 #include "permute.cuh"
 #include "quant.cuh"
 #include "route.cuh"
@@ -415,6 +416,27 @@ int launch_gemm(const GemmArgs &g, long long max_tiles, cudaStream_t s) {
     return cuda_check("ffn_gemm_kernel");
 }
 
+// The warp-level int8 grouped GEMM (comparison path): persistent, as many
+// CTAs as fit on the GPU (at most one per work item).
+template <bool GATEUP, int BITS>
+int launch_mma8(const Mma8Args &g, long long max_tiles, cudaStream_t s) {
+    using C = Mma8Cfg<GATEUP, BITS>;
+    if (C::SMEM > max_smem_optin()) return fail(MOEQ_ERR_SHAPE, "int8 GEMM needs %d bytes of shared memory", C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(ffn_mma8_kernel<GATEUP, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return fail(MOEQ_ERR_CUDA, "int8 GEMM smem attribute: %s", cudaGetErrorString(e));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_mma8_kernel<GATEUP, BITS>, kM8Threads, C::SMEM);
+    if (e != cudaSuccess || per_sm < 1) return fail(MOEQ_ERR_CUDA, "int8 GEMM occupancy query failed");
+    const long long items = max_tiles * ((GATEUP ? g.I : g.H) / C::ROWS);
+    if (items == 0) return MOEQ_OK;
+    const unsigned blocks = (unsigned)std::min<long long>(items, (long long)sm_count() * per_sm);
+    trace_begin(s);
+    ffn_mma8_kernel<GATEUP, BITS><<<blocks, kM8Threads, C::SMEM, s>>>(g);
+    trace_end(s);
+    return cuda_check("ffn_mma8_kernel");
+}
+
 // The token-to-expert permutation on the whole GPU (three small kernels).
 int permute_multi(const int32_t *idx, int T, int k, int E, int32_t *counts, int32_t *offsets, int32_t *perm_tok,
                   int32_t *perm_slot, int32_t *inv, void *ws, const Layout &L, cudaStream_t s) {
@@ -444,11 +466,51 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
         if (blocks > 0) init_y_kernel<<<blocks, 256, 0, s>>>(x, y, n, residual);
     }
     if (T == 0) return cuda_check("init_y_kernel");
+    const bool s8 = mode == MOEQ_MODE_GEMM_S8;
     plan_kernel<<<1, 1024, 0, s>>>(offsets, E, T, ctrl, mode == MOEQ_MODE_GEMV ? at<UnitRec>(ws, L.units) : nullptr,
                                    perm_tok, perm_slot, y ? w : nullptr, k, at<Tile>(ws, L.tiles),
-                                   bits == 2 ? GemmCfg<true, 2>::TILE_N : GemmCfg<true, 3>::TILE_N, at<Tile>(ws, L.tiles2),
-                                   bits == 2 ? GemmCfg<false, 2>::TILE_N : GemmCfg<false, 3>::TILE_N);
+                                   s8 ? kM8Tile : bits == 2 ? GemmCfg<true, 2>::TILE_N : GemmCfg<true, 3>::TILE_N,
+                                   at<Tile>(ws, L.tiles2),
+                                   s8 ? kM8Tile : bits == 2 ? GemmCfg<false, 2>::TILE_N : GemmCfg<false, 3>::TILE_N);
     if (int rc = cuda_check("plan_kernel")) return rc;
+    if (s8) {
+        // both GEMMs on the warp-level int8 path: x quantised per token, gate/up
+        // re-quantises h in its epilogue, down reads those int8 rows directly
+        int8_t *qx = at<int8_t>(ws, L.qx);
+        float *sx = at<float>(ws, L.sx);
+        quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                            0);
+        if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
+        const long long max_tiles = (P + kM8Tile - 1) / kM8Tile + E;
+        Mma8Args g{};
+        g.T = T;
+        g.H = H;
+        g.I = I;
+        g.E = E;
+        g.k = k;
+        for (int m = 0; m < 3; ++m) {
+            g.codes[m] = wq->codes[m];
+            g.scales[m] = wq->scales[m];
+        }
+        g.tiles = at<Tile>(ws, L.tiles);
+        g.ntiles = ctrl + 2;
+        g.perm_tok = perm_tok;
+        g.perm_slot = perm_slot;
+        g.w = w;
+        g.aq = qx;
+        g.as = sx;
+        g.qh = qh_out ? qh_out : at<int8_t>(ws, L.qh);
+        g.sh = sh_out ? sh_out : at<float>(ws, L.sh);
+        int rc = bits == 2 ? launch_mma8<true, 2>(g, max_tiles, s) : launch_mma8<true, 3>(g, max_tiles, s);
+        if (rc) return rc;
+        g.tiles = at<Tile>(ws, L.tiles2);
+        g.ntiles = ctrl + kCtrlTiles2;
+        g.aq = g.qh;
+        g.as = g.sh;
+        g.y = y;
+        g.out_sorted = out_sorted;
+        return bits == 2 ? launch_mma8<false, 2>(g, max_tiles, s) : launch_mma8<false, 3>(g, max_tiles, s);
+    }
     if (mode == MOEQ_MODE_GEMV) {
         if (out_sorted) cudaMemsetAsync(out_sorted, 0, (size_t)P * H * sizeof(float), s);
         quant_rows_kernel<<<T, 256, 0, s>>>(x, H, at<int8_t>(ws, L.qx), at<float>(ws, L.sx), nullptr, nullptr,
@@ -677,7 +739,7 @@ int moe_expert_ffn_q2(const float *x, int T, const moe_qweights *weights, int k,
     const int H = weights->H, I = weights->I, E = weights->E;
     if (int rc = check_shape(T, H, I, E, k)) return rc;
     if (int rc = check_weights(weights, H, I, E)) return rc;
-    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
+    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM_S8) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
     if (!out_sorted && !y) return fail(MOEQ_ERR_ARG, "need out_sorted or y");
     OPT_PTR(out_sorted);
     OPT_PTR(y);
@@ -705,7 +767,7 @@ int moe_shared_expert_q2(const float *x, int T, const moe_qweights *shared, floa
     if (shared->E != 1) return fail(MOEQ_ERR_ARG, "a shared expert is one expert (E = %d)", shared->E);
     if (int rc = check_shape(T, H, I, 1, 1)) return rc;
     if (int rc = check_weights(shared, H, I, 1)) return rc;
-    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
+    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM_S8) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
     if (T > 0) {
         REQ_PTR(x);
         REQ_PTR(y);
@@ -749,7 +811,7 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
     const int H = weights->H, I = weights->I, E = weights->E;
     if (int rc = check_shape(T, H, I, E, k)) return rc;
     if (int rc = check_weights(weights, H, I, E)) return rc;
-    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
+    if (mode < MOEQ_MODE_AUTO || mode > MOEQ_MODE_GEMM_S8) return fail(MOEQ_ERR_ARG, "mode = %d", mode);
     OPT_PTR(bias);
     OPT_PTR(idx_out);
     OPT_PTR(w_out);

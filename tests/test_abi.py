@@ -107,7 +107,7 @@ def test_argument_errors_are_reported_before_launch(L):
     q.E = 1
     rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), None, 0, 0, P(256), 1 << 40, None)
     assert rc == -1 and b"y is NULL" in L.moe_last_error_string()
-    rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), P(256), 1, 3, P(256), 1 << 40, None)
+    rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), P(256), 1, 4, P(256), 1 << 40, None)
     assert rc == -1
     rc = L.moe_shared_expert_q2(P(256), 4, ctypes.byref(q), P(256), 1, 0, P(256), 16, None)
     assert rc == -4

@@ -15,7 +15,9 @@ which rounds toward zero at each step: relative error up to 256 * 2^-24 per
 accumulator (~1.5e-5, measured 2.7e-5 on G*U), i.e. |dh/s| up to 127 * 3e-5
 ~ 4e-3.  With 3-bit weights the tensor-core path splits the weight panel into
 fp16 hi + lo as well and spends 3 MMAs per product (384 per accumulator), so
-its bound grows by 3/2 to ~6e-3.
+its bound grows by 3/2 to ~6e-3.  The warp-level int8 path (mode 3) forms the
+same exact integer block dots as the GEMV path and scales them with fp32 FMAs,
+so it shares the GEMV bound for either bit width.
 """
 import numpy as np
 import pytest
@@ -29,8 +31,8 @@ pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
 W_REL = 1e-5
-DELTA = {1: 1e-3, 2: 4e-3}  # GEMV, tensor-core GEMM
-DELTA3 = {1: 1e-3, 2: 6e-3}  # the same with 3-bit weights
+DELTA = {1: 1e-3, 2: 4e-3, 3: 1e-3}  # GEMV, tcgen05 GEMM, warp-level int8 GEMM
+DELTA3 = {1: 1e-3, 2: 6e-3, 3: 1e-3}  # the same with 3-bit weights
 
 
 def _w_close(w_dev, w_ref):
@@ -229,7 +231,7 @@ def _check_h_codes(ref, qh_dev, sh_dev, inv, delta):
     return int(bad.sum())
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2, 3])
 @pytest.mark.parametrize("T", [64, 600])
 def test_expert_ffn_tiny(tiny, cuda_lib, mode, T):
     x, idx, w, perm, out = _expert_case(tiny, cuda_lib, T, mode)
@@ -242,9 +244,9 @@ def test_expert_ffn_tiny(tiny, cuda_lib, mode, T):
     assert np.abs(y2.cpu().numpy() - out["y"].cpu().numpy()).max() <= 1e-5 * float(out["y"].abs().max())
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2, 3])
 def test_expert_ffn_full_sampled(full_skew, cuda_lib, mode):
-    T = 4096 if mode == 2 else 256
+    T = 256 if mode == 1 else 4096
     x, idx, w, perm, out = _expert_case(full_skew, cuda_lib, T, mode, seed=7)
     counts = perm["counts"].cpu().numpy()
     assert (counts == 0).any(), "the skewed router must leave some experts without tokens"
@@ -256,7 +258,7 @@ def test_expert_ffn_full_sampled(full_skew, cuda_lib, mode):
     full_skew.check_y(out["y"].cpu().numpy()[tokens], ref, delta=DELTA[mode])
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2, 3])
 def test_expert_ffn_tiny_3bit(tiny3, cuda_lib, mode):
     T = 600
     x, idx, w, perm, out = _expert_case(tiny3, cuda_lib, T, mode)
@@ -266,7 +268,7 @@ def test_expert_ffn_tiny_3bit(tiny3, cuda_lib, mode):
     tiny3.check_y(out["y"].cpu().numpy(), ref, delta=DELTA3[mode])
 
 
-@pytest.mark.parametrize("T,mode", [(8, 1), (1024, 2)])
+@pytest.mark.parametrize("T,mode", [(8, 1), (1024, 2), (1024, 3)])
 def test_expert_ffn_full_3bit(full3, cuda_lib, T, mode):
     x, idx, w, perm, out = _expert_case(full3, cuda_lib, T, mode, seed=11)
     tokens = np.arange(T, dtype=np.int32) if T <= 8 else \
@@ -298,7 +300,7 @@ def _shared_case(case, cuda_lib, T, mode, tokens=None):
     assert cuda_lib.device_status() == 0
 
 
-@pytest.mark.parametrize("T,mode", [(5, 1), (64, 1), (600, 2)])
+@pytest.mark.parametrize("T,mode", [(5, 1), (64, 1), (600, 2), (600, 3)])
 def test_shared_expert_tiny(shared_tiny, cuda_lib, T, mode):
     _shared_case(shared_tiny, cuda_lib, T, mode)
 
@@ -385,9 +387,9 @@ def test_layer_forward_prefill_full(full_skew, cuda_lib, residual):
     assert cuda_lib.device_status() == 0
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2, 3])
 def test_layer_forward_tiny_modes(tiny, cuda_lib, mode):
-    T = 4096 if mode == 2 else 256
+    T = 256 if mode == 1 else 4096
     x = tiny.x(T, seed=300)
     ws = _ws(cuda_lib, T, tiny.shape)
     y, idx, w = cuda_lib.layer_forward(x.to(_dev()), tiny.W, tiny.dev.Wr, None, tiny.shape.k, ws, mode=mode,
@@ -409,7 +411,7 @@ def test_zero_input_gives_zero_output(tiny, cuda_lib):
     T = 32
     x = torch.zeros(T, tiny.shape.H)
     ws = _ws(cuda_lib, T, tiny.shape)
-    for mode in (1, 2):
+    for mode in (1, 2, 3):
         y, idx, w = cuda_lib.layer_forward(x.to(_dev()), tiny.W, tiny.dev.Wr, None, tiny.shape.k, ws, mode=mode,
                                            want_routing=True)
         torch.cuda.synchronize()
