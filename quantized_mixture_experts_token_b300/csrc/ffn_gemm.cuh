@@ -222,6 +222,29 @@ struct GemmCfg {
     static_assert(TILE_N % 16 == 0 && TILE_N >= kTileMin && TILE_N <= kTileMax && B_BYTES % 1024 == 0, "tile shape");
 };
 
+// The MMAs of one K = 64 stage, from one thread: for each K step kk and matrix
+// m, D_m (+)= A_m,kk (TMEM) * B_kk (shared memory).  CAT: B = [hi rows; lo
+// rows] in one MMA of twice the tile's N; otherwise the hi and lo products are
+// two MMAs into the same accumulator.  NAT == 2 (3-bit) adds the weight
+// panel's lo part against B hi.  The sequence has no branch: a conditional
+// branch between tcgen05.mma instructions was measured to double their cost
+// to the issuing thread (45 -> 93 cycles at N = 32 .. 96).
+template <int NA, int NAT, int TN, bool CAT>
+__device__ __forceinline__ void mma_stage(uint32_t acc0, uint32_t ap, uint64_t dbh, uint64_t dbl, uint32_t idesc,
+                                          uint32_t accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < kGmK / 16; ++kk) {
+#pragma unroll
+        for (int m = 0; m < NA; ++m) {
+            const uint32_t at = ap + (uint32_t)(m * (kGmK / 2) + 8 * kk);
+            const uint32_t acc = acc0 + (uint32_t)(m * TN);
+            mma_f16_ta(acc, at, dbh + 2 * kk, idesc, kk ? 1u : accumulate);
+            if (!CAT) mma_f16_ta(acc, at, dbl + 2 * kk, idesc, 1u);
+            if (NAT == 2) mma_f16_ta(acc, at + (uint32_t)(NA * (kGmK / 2)), dbh + 2 * kk, idesc, 1u);
+        }
+    }
+}
+
 // Tracing builds: cycles each role spends in each wait, per CTA and kernel.
 #ifdef MOEQ_TIMELINE
 __device__ unsigned long long g_gemm_waits[2][256][16];
@@ -465,18 +488,8 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                     const uint64_t dbh = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
                     const uint64_t dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
                     const uint32_t ap = tmem + (uint32_t)(C::A_BASE + ps * C::A_COLS);
-#pragma unroll
-                    for (int kk = 0; kk < kGmK / 16; ++kk) {
-#pragma unroll
-                        for (int m = 0; m < NA; ++m) {
-                            const uint32_t at = ap + (uint32_t)(m * (kGmK / 2) + 8 * kk);
-                            const uint32_t acc = acc0 + (uint32_t)(m * TN);
-                            mma_f16_ta(acc, at, dbh + 2 * kk, idesc, (ks | kk) != 0);
-                            if (!cat) mma_f16_ta(acc, at, dbl + 2 * kk, idesc, 1u);
-                            if (C::NAT == 2)  // 3-bit: the weight panel's lo part against B hi (and lo when cat)
-                                mma_f16_ta(acc, at + (uint32_t)(NA * (kGmK / 2)), dbh + 2 * kk, idesc, 1u);
-                        }
-                    }
+                    if (cat) mma_stage<NA, C::NAT, TN, true>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                    else mma_stage<NA, C::NAT, TN, false>(acc0, ap, dbh, dbl, idesc, ks != 0);
                     mma_commit(smem_u32(&a_empty[ps]));
                     mma_commit(smem_u32(&b_empty[s]));
                     if (++s == S) {

@@ -66,11 +66,12 @@ __device__ __forceinline__ bool mbar_try_once(uint32_t bar, uint32_t parity) {
 // Thread 0 issues `stages` groups of PER_STAGE MMAs (N = n) from resident
 // operands in the order the grouped GEMM uses: for each K = 16 step, both
 // M = 128 blocks (two accumulators), and with PER_STAGE = 16 a second B image
-// (the lo half of a split operand).  with_sync adds what a pipelined GEMM does
+// (the lo half of a split operand).  WITH_SYNC adds what a pipelined GEMM does
 // per stage: two tests of (already completed) mbarriers, a tcgen05 fence and a
-// commit.
-template <int PER_STAGE>
-__global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int with_sync) {
+// commit.  Both are compile-time, so no conditional branch separates the MMAs
+// (one per MMA was measured to double their cost to the issuing thread).
+template <int PER_STAGE, bool WITH_SYNC>
+__global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages) {
     extern __shared__ unsigned char raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t full, slot_free, fin;
@@ -98,9 +99,11 @@ __global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int
         constexpr uint64_t kA = 16384 >> 4, kB = 32768 >> 4;  // descriptor strides of an A block and a B image
         const uint32_t idesc = (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
         const long long t0 = clock64();
+        uint32_t seen = 1;
         for (int g = 0; g < stages; ++g) {
-            if (with_sync) {
-                if (!(mbar_try_once(su32(&full), 0) && mbar_try_once(su32(&full), 0))) break;
+            if (WITH_SYNC) {
+                seen &= (uint32_t)mbar_try_once(su32(&full), 0);
+                seen &= (uint32_t)mbar_try_once(su32(&full), 0);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             }
 #pragma unroll
@@ -114,14 +117,15 @@ __global__ void __launch_bounds__(128, 1) umma_issue_loop(int n, int stages, int
                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tm + (uint32_t)(m * n)),
                             "l"(da + m * kA + 2 * kk), "l"(db + h * kB + 2 * kk), "r"(idesc), "r"(1)
                             : "memory");
-            if (with_sync)
+            if (WITH_SYNC)
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(&slot_free))
                              : "memory");
         }
+        if (!seen) g_umma_cycles = -2;  // the completed phase was not observed (never expected)
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(&fin)) : "memory");
         bool ok = false;  // the MMAs end within a few milliseconds; give up after about two seconds
         for (const long long tw = clock64(); !ok && clock64() - tw < 4000000000ll;) ok = mbar_try_once(su32(&fin), 0);
-        if (blockIdx.x == 0) g_umma_cycles = ok ? clock64() - t0 : -1;
+        if (blockIdx.x == 0 && seen) g_umma_cycles = ok ? clock64() - t0 : -1;
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -140,13 +144,14 @@ extern "C" int moe_peak_umma_issue(int n, int per_stage, int with_sync, double *
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -5;
     const int smem = 1024 + kUmmaBytes + 24 * 1024;  // the spare 24 KB keeps one CTA on each SM
     const int stages = 4096 / per_stage + 1;
-    if (per_stage == 8) {
-        if (cudaFuncSetAttribute(umma_issue_loop<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -5;
-        umma_issue_loop<8><<<sms, 128, smem>>>(n, stages, with_sync);
-    } else {
-        if (cudaFuncSetAttribute(umma_issue_loop<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -5;
-        umma_issue_loop<16><<<sms, 128, smem>>>(n, stages, with_sync);
-    }
+    auto launch = [&](auto kernel) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+        kernel<<<sms, 128, smem>>>(n, stages);
+        return true;
+    };
+    const bool launched = per_stage == 8 ? (with_sync ? launch(umma_issue_loop<8, true>) : launch(umma_issue_loop<8, false>))
+                                         : (with_sync ? launch(umma_issue_loop<16, true>) : launch(umma_issue_loop<16, false>));
+    if (!launched) return -5;
     long long cyc = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return -5;
     if (cudaMemcpyFromSymbol(&cyc, g_umma_cycles, sizeof cyc) != cudaSuccess || cyc <= 0) return -5;
