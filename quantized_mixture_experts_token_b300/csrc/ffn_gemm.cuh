@@ -215,7 +215,14 @@ struct GemmCfg {
     static constexpr size_t SMEM =
         1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES + 128 + STAGE_BYTES;
     static constexpr int UNPACK = 128;                   // unpack threads (warps 2 .. 5)
-    static constexpr int THREADS = 64 + UNPACK + 128;    // producer, MMA, unpack, epilogue warps
+#if defined(MOEQ_GEMM_ISSUERS)
+    static constexpr int ISSUERS = GATEUP ? MOEQ_GEMM_ISSUERS : 1;
+#else
+    static constexpr int ISSUERS = GATEUP ? 2 : 1;  // MMA-issuing threads (gate/up: one per matrix)
+#endif
+    // producer, MMA, unpack, epilogue warps (+ a second MMA warp after them:
+    // with two issuers, each issues the MMAs of one of the item's matrices)
+    static constexpr int THREADS = 64 + UNPACK + 128 + 32 * (ISSUERS - 1);
     static constexpr int PIECES = NA * 2;                // (matrix, K-block) pieces per unpack thread and stage
     static_assert(PSTAGES >= 2 && A_BASE + PSTAGES * A_COLS <= kTmemCols, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -229,13 +236,13 @@ struct GemmCfg {
 // panel's lo part against B hi.  The sequence has no branch: a conditional
 // branch between tcgen05.mma instructions was measured to double their cost
 // to the issuing thread (45 -> 93 cycles at N = 32 .. 96).
-template <int NA, int NAT, int TN, bool CAT>
+template <int NA, int M0, int M1, int NAT, int TN, bool CAT>
 __device__ __forceinline__ void mma_stage(uint32_t acc0, uint32_t ap, uint64_t dbh, uint64_t dbl, uint32_t idesc,
                                           uint32_t accumulate) {
 #pragma unroll
     for (int kk = 0; kk < kGmK / 16; ++kk) {
 #pragma unroll
-        for (int m = 0; m < NA; ++m) {
+        for (int m = M0; m < M1; ++m) {
             const uint32_t at = ap + (uint32_t)(m * (kGmK / 2) + 8 * kk);
             const uint32_t acc = acc0 + (uint32_t)(m * TN);
             mma_f16_ta(acc, at, dbh + 2 * kk, idesc, kk ? 1u : accumulate);
@@ -294,13 +301,17 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
 //              and of the tile's B rows (hi, lo: one contiguous, pre-swizzled
 //              run each per K stage) into the token slots, on mbarriers
 //   warp 1     TMEM owner; lane 0 issues the MMAs (A from TMEM, B from shared
-//              memory)
+//              memory; for gate/up those of the gate matrix)
 //   warps 2-5  unpack: codes -> fp16 level*scale, written into the TMEM panel
 //              stage with tcgen05.st; warp w writes the 32 weight rows of its
 //              TMEM lane quadrant w % 4
 //   warps 6-9  epilogue on the other accumulator buffer (TMEM lane quadrant
 //              = warp % 4), so item i's epilogue overlaps item i+1's MMAs
 //              (with one buffer, 3-bit gate/up, the MMAs wait for it)
+//   warp 10    gate/up only: lane 0 issues the up matrix's MMAs while warp 1
+//              issues the gate matrix's (a second issuing thread on another
+//              SM sub-partition); the stage and accumulator barriers then
+//              expect a commit from each
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag,
 // every role leaves its loop, copies and MMAs are drained and TMEM is freed.
 template <bool GATEUP, int BITS>
@@ -341,17 +352,17 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
         }
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&b_full[i]), 1);
-            mbar_init(smem_u32(&b_empty[i]), 1);
+            mbar_init(smem_u32(&b_empty[i]), C::ISSUERS);
         }
         for (int i = 0; i < PS; ++i) {
             mbar_init(smem_u32(&a_full[i]), C::UNPACK);
-            mbar_init(smem_u32(&a_empty[i]), 1);
+            mbar_init(smem_u32(&a_empty[i]), C::ISSUERS);
         }
         for (int i = 0; i < C::NBUF; ++i) {
-            mbar_init(smem_u32(&acc_full[i]), 1);
+            mbar_init(smem_u32(&acc_full[i]), C::ISSUERS);
             mbar_init(smem_u32(&acc_empty[i]), 128);
         }
-        mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(drain), C::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -450,7 +461,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             for (int g2 = max(0, gb - S); g2 < gb; ++g2)
                 mbar_drain(smem_u32(&b_full[g2 % S]), (g2 / S) & 1, abort_flag);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2 + C::UNPACK / 32 + 4) {
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
             MOEQ_GW_DECL;
@@ -488,8 +499,16 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                     const uint64_t dbh = d0 + (uint64_t)((s * C::SLOT_BYTES) >> 4);
                     const uint64_t dbl = dbh + (uint64_t)(C::B_BYTES >> 4);
                     const uint32_t ap = tmem + (uint32_t)(C::A_BASE + ps * C::A_COLS);
-                    if (cat) mma_stage<NA, C::NAT, TN, true>(acc0, ap, dbh, dbl, idesc, ks != 0);
-                    else mma_stage<NA, C::NAT, TN, false>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                    if (C::ISSUERS == 1) {
+                        if (cat) mma_stage<NA, 0, NA, C::NAT, TN, true>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                        else mma_stage<NA, 0, NA, C::NAT, TN, false>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                    } else if (warp == 1) {
+                        if (cat) mma_stage<NA, 0, 1, C::NAT, TN, true>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                        else mma_stage<NA, 0, 1, C::NAT, TN, false>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                    } else {
+                        if (cat) mma_stage<NA, 1, 2, C::NAT, TN, true>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                        else mma_stage<NA, 1, 2, C::NAT, TN, false>(acc0, ap, dbh, dbl, idesc, ks != 0);
+                    }
                     mma_commit(smem_u32(&a_empty[ps]));
                     mma_commit(smem_u32(&b_empty[s]));
                     if (++s == S) {
