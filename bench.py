@@ -58,8 +58,8 @@ SWEEP_T = (8, 16, 32, 64, 128, 256, 512, 1024)  # token counts of the GEMV / gro
 DECODE_LAYER_TRAFFIC = dict(bytes=4.220416e6 + 9.925376e6,
                             source=("ncu: route_gemv_kernel 4.22 MB + ffn_gemv_kernel 9.93 MB, one B=1 layer "
                                     "(profiles/route_gemv_decode_T1.md, ffn_gemv_decode_T1.md)"))
-GEMM_GU_TRAFFIC = dict(bytes=691.945728e6 + 20.323328e6,
-                       source="ncu: ffn_gemm_kernel<1,2> 691.9 MB read + 20.3 MB written (profiles/ffn_gemm_gateup_prefill_4k.md)")
+GEMM_GU_TRAFFIC = dict(bytes=688.752384e6 + 20.226048e6,
+                       source="ncu: ffn_gemm_kernel<1,2> 688.8 MB read + 20.2 MB written (profiles/ffn_gemm_gateup_prefill_4k.md)")
 
 
 # ------------------------------------------------------------------ helpers
