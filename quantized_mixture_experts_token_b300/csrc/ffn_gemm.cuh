@@ -176,7 +176,14 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lo, uint32_t lut_hi, u
 
 template <bool GATEUP, int BITS>
 struct GemmCfg {
-    static constexpr int NA = GATEUP ? 2 : 1;  // weight matrices per work item (gate + up, or down)
+#if defined(MOEQ_GEMM_DOWN_NA)
+    static constexpr int DOWN_NA = MOEQ_GEMM_DOWN_NA;
+#else
+    static constexpr int DOWN_NA = 2;  // two blocks share each stage's token rows (514 -> 479 us per 4K chunk)
+#endif
+    // weight blocks per work item: gate and up (the same 128 rows of each), or
+    // DOWN_NA consecutive 128-row blocks of down
+    static constexpr int NA = GATEUP ? 2 : DOWN_NA;
     static constexpr int BPB = 4 * BITS;
     static constexpr int NAT = BITS == 3 ? 2 : 1;  // weight panels per matrix: hi (, lo)
     // tokens per tile (MMA N): TMEM holds NBUF accumulator buffers of NA x TILE_N
@@ -185,8 +192,8 @@ struct GemmCfg {
     // tiles (half the MMAs of 64-token ones) with one accumulator buffer: its
     // epilogue then does not overlap the next item's MMAs.  Down (8 stages per
     // item, a comparatively long epilogue) has room for three
-    static constexpr int NBUF = GATEUP ? (BITS == 3 ? 1 : 2) : 3;
-    static constexpr int TILE_N = (GATEUP && BITS == 2) ? 96 : 128;
+    static constexpr int NBUF = NA == 2 ? (BITS == 3 ? 1 : 2) : 3;
+    static constexpr int TILE_N = (NA == 2 && BITS == 2) ? 96 : 128;
     static constexpr int ACC_COLS = NA * TILE_N;           // one accumulator buffer (fp32 columns)
     static constexpr int A_COLS = NAT * NA * (kGmK / 2);   // one stage of weight panels
     static constexpr int A_BASE = NBUF * ACC_COLS;         // first panel column
@@ -216,9 +223,9 @@ struct GemmCfg {
         1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES + 128 + STAGE_BYTES;
     static constexpr int UNPACK = 128;                   // unpack threads (warps 2 .. 5)
 #if defined(MOEQ_GEMM_ISSUERS)
-    static constexpr int ISSUERS = GATEUP ? MOEQ_GEMM_ISSUERS : 1;
+    static constexpr int ISSUERS = NA == 2 ? MOEQ_GEMM_ISSUERS : 1;
 #else
-    static constexpr int ISSUERS = GATEUP ? 2 : 1;  // MMA-issuing threads (gate/up: one per matrix)
+    static constexpr int ISSUERS = NA;  // MMA-issuing threads: one per weight block of an item
 #endif
     // producer, MMA, unpack, epilogue warps (+ a second MMA warp after them:
     // with two issuers, each issues the MMAs of one of the item's matrices)
@@ -318,7 +325,8 @@ template <bool GATEUP, int BITS>
 __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_kernel(const __grid_constant__ GemmArgs a) {
     using C = GemmCfg<GATEUP, BITS>;
     constexpr int NA = C::NA, BPB = C::BPB, S = C::STAGES, R = C::RSTAGES, PS = C::PSTAGES, TN = C::TILE_N;
-    const int MT = (GATEUP ? a.I : a.H) / kGmM;
+    // work items per tile; with H an odd multiple of 128 the last down item has one block
+    const int MT = GATEUP ? a.I / kGmM : (a.H + kGmM * NA - 1) / (kGmM * NA);
     const int K = GATEUP ? a.H : a.I;
     const int KB = K / 32, nk = K / kGmK;
     const int NR = GATEUP ? a.I : a.H;  // rows of each weight matrix
@@ -379,7 +387,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
 
     // work item j of this CTA -> (tile, first weight row)
     auto item_tile = [&](int j) { return a.tiles[((int)blockIdx.x + j * (int)gridDim.x) / MT]; };
-    auto item_m0 = [&](int j) { return (((int)blockIdx.x + j * (int)gridDim.x) % MT) * kGmM; };
+    auto item_m0 = [&](int j) { return (((int)blockIdx.x + j * (int)gridDim.x) % MT) * (GATEUP ? kGmM : kGmM * NA); };
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -404,12 +412,15 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                         break;
                     }
                     const uint32_t rbar = smem_u32(&raw_full[rs]);
-                    if (lane == 0) mbar_arrive_expect_tx(rbar, (uint32_t)C::RAW_BYTES);
+                    // weight blocks of this item inside the matrix (the second block of a down
+                    // item past the last row is not fetched; its panel and accumulator are unused)
+                    const int nbv = GATEUP ? NA : min(NA, (NR - rm0) / kGmM);
+                    if (lane == 0) mbar_arrive_expect_tx(rbar, (uint32_t)(C::RAW_BYTES / NA * nbv));
                     __syncwarp();
-                    if (lane < 4 * NA) {  // lanes [0, 2NA): codes of (matrix, block); [2NA, 4NA): scales
+                    if (lane < 4 * NA && ((lane % (2 * NA)) >> 1) < nbv) {  // lanes [0, 2NA): codes of (matrix, block); [2NA, 4NA): scales
                         const int mb = lane % (2 * NA), m = mb >> 1, kb = 2 * rks + (mb & 1);
                         const int mat = GATEUP ? m : 2;
-                        const size_t blk = ((size_t)rtl.e * KB + kb) * NR + rm0;
+                        const size_t blk = ((size_t)rtl.e * KB + kb) * NR + rm0 + (GATEUP ? 0 : m * kGmM);
                         unsigned char *rw = raws + (size_t)rs * C::RAW_BYTES;
                         if (lane < 2 * NA)
                             bulk_g2s(smem_u32(rw + mb * kGmM * BPB), a.codes[mat] + blk * BPB, kGmM * BPB, rbar, pol);
@@ -658,12 +669,17 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
             const int *etab = s_exp + buf * TN;
             const uint32_t acc = tl_lane + (uint32_t)(buf * C::ACC_COLS);
             const bool cat = nround <= TN / 2;  // lo products in columns [nround, 2 nround) (MMA warp)
+            // down: one pass per 128-row block of the item (accumulator m); gate/up: one pass
+            const int nbv = GATEUP ? 1 : min(NA, (a.H - m0) / kGmM);
+            for (int mb = 0; mb < nbv; ++mb) {
+            const uint32_t accm = acc + (uint32_t)(mb * TN);
+            const int r0 = m0 + mb * kGmM;  // first weight row of this pass
             for (int c0 = 0; c0 < nround; c0 += 16) {
                 float acc0[16];
-                tmem_ld16(acc + (uint32_t)c0, acc0);
+                tmem_ld16(accm + (uint32_t)c0, acc0);
                 if (cat) {
                     float lo0[16];
-                    tmem_ld16(acc + (uint32_t)(nround + c0), lo0);
+                    tmem_ld16(accm + (uint32_t)(nround + c0), lo0);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) acc0[jj] += lo0[jj];
                 }
@@ -695,7 +711,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                     if (a.y) {
                         // w * D of these 16 pairs -> this warp's staging buffer [pair][its 32
                         // rows] -> one 128-byte bulk reduction per pair into
-                        // y[token][m0 + 32 (warp % 4) ...]; warps proceed independently
+                        // y[token][r0 + 32 (warp % 4) ...]; warps proceed independently
                         const int q = warp & 3;
                         float *stg = s_stage + ((nstage & 1) * 4 + q) * 16 * 32;
                         bulk_wait_read<1>();  // (issuing lanes) this buffer's previous reductions have read it
@@ -709,7 +725,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                         __syncwarp();
                         if (lane < 16) {
                             if (c0 + lane < nval)
-                                bulk_reduce_add_f32(a.y + (size_t)ttab[c0 + lane] * a.H + m0 + 32 * q,
+                                bulk_reduce_add_f32(a.y + (size_t)ttab[c0 + lane] * a.H + r0 + 32 * q,
                                                     smem_u32(stg + lane * 32), 32 * 4);
                             bulk_commit();
                         }
@@ -720,10 +736,11 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                         for (int jj = 0; jj < 16; ++jj) {
                             const int jc = c0 + jj;
                             if (jc >= nval) break;
-                            a.out_sorted[(size_t)(p0 + jc) * a.H + m0 + row] = acc0[jj] * exp2i(etab[jc]);
+                            a.out_sorted[(size_t)(p0 + jc) * a.H + r0 + row] = acc0[jj] * exp2i(etab[jc]);
                         }
                     }
                 }
+            }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[buf]));

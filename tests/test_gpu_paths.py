@@ -222,18 +222,20 @@ def test_combine_against_oracle(request, cuda_lib, case_name, T, residual):
     assert cuda_lib.device_status() == 0
 
 
-@pytest.mark.parametrize("H,T", [(384, 37), (256, 3)])
-def test_gemv_other_hidden_sizes(cuda_lib, H, T):
-    """The decode expert kernel at hidden sizes other than the model's (12 and 8
-    K-blocks), with more tokens than one pass holds (T = 37)."""
+@pytest.mark.parametrize("H,T,mode", [(384, 37, 1), (256, 3, 1), (384, 600, 2), (384, 600, 3)])
+def test_other_hidden_sizes(cuda_lib, H, T, mode):
+    """The expert kernels at hidden sizes other than the model's (12 and 8
+    K-blocks): the decode kernel with more tokens than one pass holds (T = 37),
+    and the grouped GEMMs with H an odd multiple of 128 (the tcgen05 down GEMM's
+    last item then holds one 128-row block instead of two)."""
     shape = synth.LayerShape(H=H, I=128, E=8, k=2)
     case = LayerCase(shape, seed=31, device="cpu")
     x = case.x(T, seed=900 + H)
     ws = _ws(cuda_lib, T, shape)
-    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), case.W, case.dev.Wr, None, shape.k, ws, mode=1,
+    y, idx, w = cuda_lib.layer_forward(x.to(_dev()), case.W, case.dev.Wr, None, shape.k, ws, mode=mode,
                                        want_routing=True)
     torch.cuda.synchronize()
     ref = case.oracle(x)
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
-    case.check_y(y.cpu().numpy(), ref, delta=DELTA[1])
+    case.check_y(y.cpu().numpy(), ref, delta=DELTA[mode])
     assert cuda_lib.device_status() == 0
