@@ -386,29 +386,8 @@ def prefill_chunk(gpu, pre_layer, preW, args, rank):
     tf32_peak = pk["bf16"] / 2.0  # tf32 dense rate is half the bf16 rate (nominal 1.1 vs 2.25 PFLOP/s)
     s8 = s8_peak_tops()
 
-    # the same chunk with both expert GEMMs on the warp-level int8 path
-    # (exact block products scaled in registers): the comparison point
-    def call_s8():
-        moeq.layer_forward(xp, preW, pre_layer.Wr, pre_layer.bias, K_TOP, wsp, y=yp, mode=moeq.MODE_GEMM_S8)
-
-    g8 = gpu.graph(call_s8)
-    ev8 = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    moeq.trace_events(ev8)
-    g8_tr = gpu.graph(call_s8)
-    moeq.trace_events(None)
-    pre8 = aggregate(Tp * psteps, gpu.timed(g8.replay, psteps, args.warmup), gpu.world)
-    for _ in range(3):
-        g8_tr.replay()
-    torch.cuda.synchronize()
-    gu8_s, dn8_s = (ev8[2 * i].elapsed_time(ev8[2 * i + 1]) / 1e3 for i in (1, 2))
-    s8_path = dict(
-        kernel="ffn_mma8_kernel: mma.sync m16n8k32 s8, every 32-block product an exact integer dot scaled in registers",
-        value=pre8["value"], unit="tokens/s", ms_per_chunk=1e3 * pre8["seconds"] / psteps,
-        gateup=dict(launch_us=gu8_s * 1e6, achieved_tops=gu_flop / gu8_s / 1e12,
-                    frac_of_s8=(gu_flop / gu8_s / 1e12 / s8) if s8 else None),
-        down=dict(launch_us=dn8_s * 1e6, achieved_tops=dn_flop / dn8_s / 1e12,
-                  frac_of_s8=(dn_flop / dn8_s / 1e12 / s8) if s8 else None),
-        s8_peak_tops=s8)
+    s8_path = None if args.no_s8 else s8_chunk(gpu, call_args=(xp, preW, pre_layer, wsp, yp), psteps=psteps,
+                                               args=args, s8=s8, gu_flop=gu_flop, dn_flop=dn_flop)
     return dict(
         value=pre["value"], unit="tokens/s", ms_per_chunk=1e3 * pre["seconds"] / psteps,
         workload="prefill: 4,096-token chunk through one 2048/512/512 top-10 2-bit layer, Zipf(1.1)-skewed router",
@@ -428,6 +407,36 @@ def prefill_chunk(gpu, pre_layer, preW, args, rank):
                                   peak_source="tf32 = measured bf16 / 2")),
         e2e=dict(value=pe["value"], unit="tokens/s", h2d_bytes_per_step=Tp * H * 4, d2h_bytes_per_step=Tp * H * 4),
         s8_path=s8_path)
+
+
+def s8_chunk(gpu, call_args, psteps, args, s8, gu_flop, dn_flop):
+    """The same chunk with both expert GEMMs on the warp-level int8 path (exact
+    block products scaled in registers): the comparison point."""
+    torch, moeq = gpu.torch, gpu.moeq
+    xp, preW, pre_layer, wsp, yp = call_args
+    Tp = xp.shape[0]
+
+    def call_s8():
+        moeq.layer_forward(xp, preW, pre_layer.Wr, pre_layer.bias, K_TOP, wsp, y=yp, mode=moeq.MODE_GEMM_S8)
+
+    g8 = gpu.graph(call_s8)
+    ev8 = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    moeq.trace_events(ev8)
+    g8_tr = gpu.graph(call_s8)
+    moeq.trace_events(None)
+    pre8 = aggregate(Tp * psteps, gpu.timed(g8.replay, psteps, args.warmup), gpu.world)
+    for _ in range(3):
+        g8_tr.replay()
+    torch.cuda.synchronize()
+    gu8_s, dn8_s = (ev8[2 * i].elapsed_time(ev8[2 * i + 1]) / 1e3 for i in (1, 2))
+    return dict(
+        kernel="ffn_mma8_kernel: mma.sync m16n8k32 s8, every 32-block product an exact integer dot scaled in registers",
+        value=pre8["value"], unit="tokens/s", ms_per_chunk=1e3 * pre8["seconds"] / psteps,
+        gateup=dict(launch_us=gu8_s * 1e6, achieved_tops=gu_flop / gu8_s / 1e12,
+                    frac_of_s8=(gu_flop / gu8_s / 1e12 / s8) if s8 else None),
+        down=dict(launch_us=dn8_s * 1e6, achieved_tops=dn_flop / dn8_s / 1e12,
+                  frac_of_s8=(dn_flop / dn8_s / 1e12 / s8) if s8 else None),
+        s8_peak_tops=s8)
 
 
 def stack_prompt(gpu, layers, Ws, args, rank):
@@ -633,6 +642,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--stack-reps", type=int, default=2)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-s8", action="store_true", help="skip the int8 comparison leg of the prefill chunk")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-3bit", action="store_true")
