@@ -179,7 +179,10 @@ struct GemmCfg {
 #if defined(MOEQ_GEMM_DOWN_NA)
     static constexpr int DOWN_NA = MOEQ_GEMM_DOWN_NA;
 #else
-    static constexpr int DOWN_NA = 2;  // two blocks share each stage's token rows (514 -> 479 us per 4K chunk)
+    // 2-bit: two blocks share each stage's token rows (514 -> 485 us per 4K chunk).
+    // 3-bit keeps one: two would leave TMEM room for a single accumulator buffer
+    // (16K-token 3-bit chunk 6.9 -> 7.9 ms)
+    static constexpr int DOWN_NA = BITS == 2 ? 2 : 1;
 #endif
     // weight blocks per work item: gate and up (the same 128 rows of each), or
     // DOWN_NA consecutive 128-row blocks of down
