@@ -455,7 +455,8 @@ int permute_multi(const int32_t *idx, int T, int k, int E, int32_t *counts, int3
 // Experts over an existing permutation.
 int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t *offsets, const int32_t *perm_tok,
             const int32_t *perm_slot, const float *w, float *out_sorted, float *y, int residual, int mode,
-            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, cudaStream_t s, bool init_y = true) {
+            int8_t *qh_out, float *sh_out, void *ws, const Layout &L, cudaStream_t s, bool init_y = true,
+            const int32_t *inv = nullptr) {
     const int H = wq->H, I = wq->I, E = wq->E, bits = wq->bits;
     const long long P = (long long)T * k;
     if (mode == MOEQ_MODE_AUTO) mode = T <= kExpertGemvMaxT ? MOEQ_MODE_GEMV : MOEQ_MODE_GEMM;
@@ -543,8 +544,6 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
         return gemv_dispatch(g, bits, T, k, E, s);
     }
     // grouped tensor-core GEMMs
-    int8_t *qx = at<int8_t>(ws, L.qx);
-    float *sx = at<float>(ws, L.sx);
     int *ex = at<int>(ws, L.ex);
     __half *ximg = at<__half>(ws, L.ximg);
     int8_t *qh = qh_out ? qh_out : at<int8_t>(ws, L.qh);
@@ -552,14 +551,22 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
     int *eh = at<int>(ws, L.eh);
     __half *himg = at<__half>(ws, L.himg);
     const long long img_rows = P + kTileMax;  // a tile's rows may run up to kTileMax - 1 past P
-    // x quantised per token, then its fp16 hi/lo rows written in sorted pair
-    // order (pre-swizzled per tile) so that every GEMM tile reads one
-    // contiguous run of B rows per K stage
-    quant_rows_kernel<<<T, 256, 0, s>>>(x, H, qx, sx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0);
-    if (int rc = cuda_check("quant_rows_kernel(x)")) return rc;
+    // x quantised per token and its fp16 hi/lo rows written in sorted pair
+    // order (pre-swizzled per tile), in one pass, so that every GEMM tile reads
+    // one contiguous run of B rows per K stage.  The pairs' sorted positions
+    // come from the permutation's inverse (computed here when not given).
+    if (!inv) {
+        int32_t *winv = at<int32_t>(ws, L.inv);
+        cudaMemsetAsync(winv, 0xFF, (size_t)P * sizeof(int32_t), s);  // -1: a pair the permutation rejected
+        const unsigned pr_blocks = (unsigned)std::min<long long>((P + 255) / 256, (long long)sm_count() * 8);
+        pair_rows_kernel<<<pr_blocks, 256, 0, s>>>(perm_tok, perm_slot, (int)P, T, k, winv);
+        if (int rc = cuda_check("pair_rows_kernel")) return rc;
+        inv = winv;
+    }
+    const unsigned qs_blocks = (unsigned)std::min<long long>(((long long)T + 7) / 8, (long long)sm_count() * 16);
+    quant_split_kernel<<<qs_blocks, 256, 0, s>>>(x, T, H, k, inv, offsets, E, ximg, img_rows, ex);
+    if (int rc = cuda_check("quant_split_kernel")) return rc;
     const unsigned split_blocks = (unsigned)std::min<long long>((P + 7) / 8, (long long)sm_count() * 16);
-    split_rows_kernel<<<split_blocks, 256, 0, s>>>(qx, sx, H, perm_tok, (int)P, T, offsets, E, ximg, img_rows, ex);
-    if (int rc = cuda_check("split_rows_kernel(x)")) return rc;
     const long long max_tiles = (P + kTileMin - 1) / kTileMin + E;
     GemmArgs g{};
     g.T = T;
@@ -886,7 +893,7 @@ int moe_layer_forward(const float *x, int T, const float *Wr, const float *bias,
     if (int rc = cuda_check("route")) return rc;
     if (int rc = permute_multi(idx, T, k, E, counts, offsets, perm_tok, perm_slot, inv, ws, L, s)) return rc;
     if (int rc = experts(x, T, weights, k, offsets, perm_tok, perm_slot, w, nullptr, y_out, residual, mode, nullptr,
-                         nullptr, ws, L, s))
+                         nullptr, ws, L, s, true, inv))
         return rc;
     return ok();
 }

@@ -145,4 +145,96 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const int8_t *__restric
     }
 }
 
+// The x operand image of the grouped GEMM straight from x: for every token t
+// (one warp), its row is quantised per 32-block by the rule of
+// quant_rows_kernel and the resulting q*s*2^-e values, split into fp16 hi +
+// lo, are written to the image rows inv[t*k + j] of all its k pairs (rows
+// that split_rows_kernel would write from q and s, bit for bit), with
+// e_out[row] = e.  Two passes over the row: the block scales and their
+// maximum (the row exponent e), then the codes and the image.  Lane l holds
+// values 4l .. 4l + 3 of each 128-value group, so eight lanes make a block
+// and two lanes one 16-byte chunk (each stores its 8 bytes).  inv < 0: a
+// pair the permutation rejected (not written).
+__global__ void __launch_bounds__(256) quant_split_kernel(const float *__restrict__ x, int T, int H, int k,
+                                                          const int32_t *__restrict__ inv,
+                                                          const int32_t *__restrict__ offsets, int E,
+                                                          __half *__restrict__ img, long long img_rows,
+                                                          int *__restrict__ e_out) {
+    const int lane = threadIdx.x & 31;
+    const size_t half_stride = (size_t)img_rows * 64;  // elements of one (stage, half) plane
+    const int NG = H / 128;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+        const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)t * H) + lane;
+        // pass 1: the row's largest block scale
+        float smax = 0.f;
+        for (int g = 0; g < NG; ++g) {
+            const float4 v = xr[32 * g];
+            float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            smax = fmaxf(smax, block_scale(a));
+        }
+        smax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(smax)));
+        const int e = row_exponent(smax);
+        const float inv2 = exp2i(-e);
+        // the image row of pair j (lane j) and its swizzle phase: (row - first row of its expert) & 7
+        int prow = -1;
+        uint32_t phase = 0;
+        if (lane < k) {
+            prow = inv[(size_t)t * k + lane];
+            if (prow >= 0) {
+                int lo_e = 0, hi_e = E;  // the last e with offsets[e] <= prow
+                while (hi_e - lo_e > 1) {
+                    const int mid = (lo_e + hi_e) >> 1;
+                    if (offsets[mid] <= prow) lo_e = mid;
+                    else hi_e = mid;
+                }
+                phase = (uint32_t)(prow - offsets[lo_e]) & 7u;
+                e_out[prow] = e;
+            }
+        }
+        // pass 2: codes, the hi/lo split, and the stores to every pair row
+        for (int g = 0; g < NG; ++g) {
+            const float4 v = xr[32 * g];
+            float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float s = block_scale(a);
+            const float sc = s * inv2;
+            const float vals[4] = {v.x, v.y, v.z, v.w};
+            uint32_t hw[2], lw[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                __half h0, l0, h1, l1;
+                split_hi_lo((float)block_code(vals[2 * i], s) * sc, h0, l0);
+                split_hi_lo((float)block_code(vals[2 * i + 1], s) * sc, h1, l1);
+                hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+                lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            }
+            const int c = 16 * g + (lane >> 1);  // 16-byte chunk of the row
+            const size_t st = (size_t)(c >> 3);
+            const uint32_t cc = (uint32_t)c & 7u;
+            for (int j = 0; j < k; ++j) {
+                const int r = __shfl_sync(0xffffffffu, prow, j);
+                const uint32_t ph = __shfl_sync(0xffffffffu, phase, j);
+                if (r < 0) continue;
+                const size_t off = (size_t)r * 64 + ((cc ^ ph) << 3) + 4 * (lane & 1);
+                *reinterpret_cast<uint2 *>(img + (2 * st) * half_stride + off) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2 *>(img + (2 * st + 1) * half_stride + off) = make_uint2(lw[0], lw[1]);
+            }
+        }
+    }
+}
+
+// inv[t*k + j] = the sorted position of pair (t, j), from the permutation's
+// perm_tok / perm_slot (inv filled with -1 beforehand: rejected pairs stay so).
+__global__ void __launch_bounds__(256) pair_rows_kernel(const int32_t *__restrict__ perm_tok,
+                                                        const int32_t *__restrict__ perm_slot, int P, int T, int k,
+                                                        int32_t *__restrict__ inv) {
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < P; r += gridDim.x * blockDim.x) {
+        const int t = perm_tok[r], j = perm_slot[r];
+        if (t >= 0 && t < T && j >= 0 && j < k) inv[(size_t)t * k + j] = r;
+    }
+}
+
 }  // namespace moeq
