@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                 float wv = 0.f;
                 if (t < 0 || t >= a.T || js < 0 || js >= a.k) {  // a caller's bad permutation: no contribution
                     set_status(MOEQ_STATUS_BAD_INDEX);
-                    t = -1;  // its operand row holds no defined values: every output of the pair is skipped
+                    t = 0;
                 } else if (!GATEUP && a.w) {
                     wv = a.w[(size_t)t * a.k + js];
                 }
@@ -699,10 +699,9 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                     for (int jj = 0; jj < 16; ++jj) {
                         const int jc = c0 + jj;
                         if (jc >= nval) break;
-                        const bool okp = s_tok[buf * TN + jc] >= 0;  // uniform over the warp
                         const float sc = exp2i(etab[jc]);
                         const float Gv = acc0[jj] * sc, Uv = acc1[jj] * sc;
-                        const float h = okp ? __fdiv_rn(Gv, 1.0f + expf(-Gv)) * Uv : 0.0f;
+                        const float h = __fdiv_rn(Gv, 1.0f + expf(-Gv)) * Uv;
                         const float s = block_scale(warp_absmax(h));
                         const int q = block_code(h, s);
                         const size_t p = (size_t)(p0 + jc);
@@ -723,12 +722,12 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
                             const int jc = c0 + jj;
-                            stg[jj * 32 + lane] = ttab[jc] >= 0 ? wtab[jc] * acc0[jj] * exp2i(etab[jc]) : 0.0f;
+                            stg[jj * 32 + lane] = wtab[jc] * acc0[jj] * exp2i(etab[jc]);
                         }
                         fence_proxy_async();
                         __syncwarp();
                         if (lane < 16) {
-                            if (c0 + lane < nval && ttab[c0 + lane] >= 0)
+                            if (c0 + lane < nval)
                                 bulk_reduce_add_f32(a.y + (size_t)ttab[c0 + lane] * a.H + r0 + 32 * q,
                                                     smem_u32(stg + lane * 32), 32 * 4);
                             bulk_commit();
@@ -740,8 +739,7 @@ __global__ void __launch_bounds__(GemmCfg<GATEUP, BITS>::THREADS, 1) ffn_gemm_ke
                         for (int jj = 0; jj < 16; ++jj) {
                             const int jc = c0 + jj;
                             if (jc >= nval) break;
-                            a.out_sorted[(size_t)(p0 + jc) * a.H + r0 + row] =
-                                ttab[jc] >= 0 ? acc0[jj] * exp2i(etab[jc]) : 0.0f;
+                            a.out_sorted[(size_t)(p0 + jc) * a.H + r0 + row] = acc0[jj] * exp2i(etab[jc]);
                         }
                     }
                 }

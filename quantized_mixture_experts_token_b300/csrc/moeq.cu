@@ -562,6 +562,10 @@ int experts(const float *x, int T, const moe_qweights *wq, int k, const int32_t 
         pair_rows_kernel<<<pr_blocks, 256, 0, s>>>(perm_tok, perm_slot, (int)P, T, k, winv);
         if (int rc = cuda_check("pair_rows_kernel")) return rc;
         inv = winv;
+        // rows of a caller's inconsistent permutation that no pair claims: zeroed
+        const unsigned or_blocks = (unsigned)std::min<long long>((P + 7) / 8, (long long)sm_count() * 16);
+        orphan_rows_kernel<<<or_blocks, 256, 0, s>>>(perm_tok, perm_slot, (int)P, T, k, inv, H, ximg, img_rows, ex);
+        if (int rc = cuda_check("orphan_rows_kernel")) return rc;
     }
     const unsigned qs_blocks = (unsigned)std::min<long long>(((long long)T + 7) / 8, (long long)sm_count() * 16);
     quant_split_kernel<<<qs_blocks, 256, 0, s>>>(x, T, H, k, inv, offsets, E, ximg, img_rows, ex);

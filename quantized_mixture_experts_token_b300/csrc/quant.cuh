@@ -237,4 +237,26 @@ __global__ void __launch_bounds__(256) pair_rows_kernel(const int32_t *__restric
     }
 }
 
+// The x image rows of sorted positions that no pair's inverse points back to
+// (a caller's permutation with out-of-range or repeated entries): zeroed, with
+// exponent 0, so that the GEMMs only ever read defined operand rows.  One warp
+// per sorted position; a no-op for a consistent permutation.
+__global__ void __launch_bounds__(256) orphan_rows_kernel(const int32_t *__restrict__ perm_tok,
+                                                          const int32_t *__restrict__ perm_slot, int P, int T, int k,
+                                                          const int32_t *__restrict__ inv, int H,
+                                                          __half *__restrict__ img, long long img_rows,
+                                                          int *__restrict__ e_out) {
+    const int lane = threadIdx.x & 31;
+    const size_t half_stride = (size_t)img_rows * 64;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < P; r += (gridDim.x * blockDim.x) >> 5) {
+        const int t = perm_tok[r], j = perm_slot[r];
+        const bool claimed = t >= 0 && t < T && j >= 0 && j < k && inv[(size_t)t * k + j] == r;
+        if (claimed) continue;  // uniform over the warp
+        if (lane == 0) e_out[r] = 0;
+        for (int c = lane; c < 2 * (H / 64) * 8; c += 32)  // (stage, half) plane c / 8, 16-byte chunk c % 8
+            *reinterpret_cast<uint4 *>(img + (size_t)(c >> 3) * half_stride + (size_t)r * 64 + (c & 7) * 8) =
+                make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 }  // namespace moeq
