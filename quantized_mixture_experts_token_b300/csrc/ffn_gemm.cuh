@@ -176,14 +176,10 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lo, uint32_t lut_hi, u
 
 template <bool GATEUP, int BITS>
 struct GemmCfg {
-#if defined(MOEQ_GEMM_DOWN_NA)
-    static constexpr int DOWN_NA = MOEQ_GEMM_DOWN_NA;
-#else
     // 2-bit: two blocks share each stage's token rows (514 -> 485 us per 4K chunk).
     // 3-bit keeps one: two would leave TMEM room for a single accumulator buffer
     // (16K-token 3-bit chunk 6.9 -> 7.9 ms)
     static constexpr int DOWN_NA = BITS == 2 ? 2 : 1;
-#endif
     // weight blocks per work item: gate and up (the same 128 rows of each), or
     // DOWN_NA consecutive 128-row blocks of down
     static constexpr int NA = GATEUP ? 2 : DOWN_NA;
@@ -225,11 +221,7 @@ struct GemmCfg {
     static constexpr size_t SMEM =
         1024 + (size_t)STAGES * SLOT_BYTES + (size_t)RSTAGES * RAW_BYTES + MISC_BYTES + 128 + STAGE_BYTES;
     static constexpr int UNPACK = 128;                   // unpack threads (warps 2 .. 5)
-#if defined(MOEQ_GEMM_ISSUERS)
-    static constexpr int ISSUERS = NA == 2 ? MOEQ_GEMM_ISSUERS : 1;
-#else
     static constexpr int ISSUERS = NA;  // MMA-issuing threads: one per weight block of an item
-#endif
     // producer, MMA, unpack, epilogue warps (+ a second MMA warp after them:
     // with two issuers, each issues the MMAs of one of the item's matrices)
     static constexpr int THREADS = 64 + UNPACK + 128 + 32 * (ISSUERS - 1);
@@ -311,16 +303,17 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
 //              and of the tile's B rows (hi, lo: one contiguous, pre-swizzled
 //              run each per K stage) into the token slots, on mbarriers
 //   warp 1     TMEM owner; lane 0 issues the MMAs (A from TMEM, B from shared
-//              memory; for gate/up those of the gate matrix)
+//              memory; with two weight blocks per item, those of the first)
 //   warps 2-5  unpack: codes -> fp16 level*scale, written into the TMEM panel
 //              stage with tcgen05.st; warp w writes the 32 weight rows of its
 //              TMEM lane quadrant w % 4
 //   warps 6-9  epilogue on the other accumulator buffer (TMEM lane quadrant
 //              = warp % 4), so item i's epilogue overlaps item i+1's MMAs
 //              (with one buffer, 3-bit gate/up, the MMAs wait for it)
-//   warp 10    gate/up only: lane 0 issues the up matrix's MMAs while warp 1
-//              issues the gate matrix's (a second issuing thread on another
-//              SM sub-partition); the stage and accumulator barriers then
+//   warp 10    items of two weight blocks (gate/up; 2-bit down): lane 0
+//              issues the second block's MMAs while warp 1 issues the
+//              first's (a second issuing thread on another SM
+//              sub-partition); the stage and accumulator barriers then
 //              expect a commit from each
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag,
 // every role leaves its loop, copies and MMAs are drained and TMEM is freed.
