@@ -220,28 +220,73 @@ __device__ __forceinline__ void route_accumulate(float (&acc)[kRouteRows][AT], c
 #pragma unroll
         for (int r = 0; r < kRouteRows; ++r)
             wv[r] = r < nr ? *reinterpret_cast<const float4 *>(wr + r * hc + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+        // the tokens' x values first, all in flight at once (a load behind each
+        // token's branch would wait out one L2 latency per token); a slot past the
+        // call's tokens reads token t0 and is not used
+        float4 xv[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            xv[t] = *reinterpret_cast<const float4 *>(x + (size_t)(t0 + (t < nt ? t : 0)) * H + c0 + h);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             if (t < nt) {
-                const float4 xv = *reinterpret_cast<const float4 *>(x + (size_t)(t0 + t) * H + c0 + h);
 #pragma unroll
                 for (int r = 0; r < kRouteRows; ++r)
-                    acc[r][t] = fmaf(wv[r].x, xv.x, fmaf(wv[r].y, xv.y, fmaf(wv[r].z, xv.z, fmaf(wv[r].w, xv.w, acc[r][t]))));
+                    acc[r][t] = fmaf(wv[r].x, xv[t].x,
+                                     fmaf(wv[r].y, xv[t].y, fmaf(wv[r].z, xv[t].z, fmaf(wv[r].w, xv[t].w, acc[r][t]))));
             }
         }
     }
 }
 
+// Warp sums of V <= 32 values per lane at once (a reduce-scatter): each step
+// sends half of the remaining values to the lane `o` away and keeps the half
+// selected by that lane bit, so after log2(V) steps lane l holds a partial of
+// value l >> (5 - log2 V), completed by xor-sums over the remaining lane bits.
+// 31 shuffles for 32 values, where one warp sum each would take 160.
+template <int V>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
+    static_assert(V >= 2 && V <= 32 && (V & (V - 1)) == 0, "V a power of two <= 32");
+#pragma unroll
+    for (int n = V, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float mine = up ? v[n / 2 + i] : v[i];
+            const float other = up ? v[i] : v[n / 2 + i];
+            v[i] = mine + __shfl_xor_sync(0xffffffffu, other, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 / V; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
 template <int NT, int AT>
 __device__ __forceinline__ void route_reduce(const float (&acc)[kRouteRows][AT], float (*part)[kRouteRows][kRouteTok],
                                              int warp, int lane) {
+    if (NT == 1) {
 #pragma unroll
-    for (int r = 0; r < kRouteRows; ++r)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const float s = warp_sum(acc[r][t]);
-            if (lane == 0) part[warp][r][t] = s;
+        for (int r = 0; r < kRouteRows; ++r) {
+            const float s = warp_sum(acc[r][0]);
+            if (lane == 0) part[warp][r][0] = s;
         }
+        return;
+    }
+    // value i = r * NT + t, reduced in groups of at most 32 values
+    constexpr int V = kRouteRows * NT, G = V > 32 ? 32 : V, LG = G == 32 ? 5 : G == 16 ? 4 : G == 8 ? 3 : 2;
+#pragma unroll
+    for (int g0 = 0; g0 < V; g0 += G) {
+        float v[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) v[i] = acc[(g0 + i) / NT][(g0 + i) % NT];
+        const float s = warp_reduce_scatter<G>(v, lane);
+        if ((lane & ((32 >> LG) - 1)) == 0) {
+            const int i = g0 + (lane >> (5 - LG));
+            part[warp][i / NT][i % NT] = s;
+        }
+    }
 }
 
 // MAXT: the most tokens of a call (1 or kRouteTok).  The single-token
